@@ -1,0 +1,144 @@
+"""Exact attention on NVIDIA GB300: Python binding of the C-ABI library.
+
+The functions here carry the names of the C entry points in include/fa.h and
+only marshal arguments: they check dtypes and shapes of PyTorch tensors, pass
+their device pointers and the current CUDA stream to libfa.so, and turn a
+non-zero status into `FaError`.  Every step of the computation runs in the
+library's CUDA kernels; there is no other implementation behind these calls.
+If libfa.so is missing or cannot be loaded, importing the binding succeeds but
+every call raises.
+
+    o, lse = attention_forward(q, k, v, causal=True)
+    dq, dk, dv = attention_backward(q, k, v, o, lse, do, causal=True)
+"""
+
+import ctypes
+import math
+
+from ._lib import FaError, library, status_string  # noqa: F401
+
+__all__ = [
+    "FaError", "fa_forward", "fa_backward", "fa_backward_preprocess", "fa_status_string",
+    "fa_last_device_error", "fa_selftest_wait_timeout", "attention_forward", "attention_backward",
+    "library",
+]
+
+FA_OK = 0
+FA_ERR_INVALID_ARGUMENT = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_DEVICE_TIMEOUT = 4
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, what):
+    if status != FA_OK:
+        raise FaError(status, what)
+
+
+def _bf16_cuda(name, t, shape=None):
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _f32_cuda(name, t, shape):
+    import torch
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _shapes(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be [B, H, N, d]")
+    B, Hq, N, d = q.shape
+    if k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError("k must be [B, H_kv, N, d] with q's B, N and d")
+    return B, Hq, k.shape[1], N, d
+
+
+def fa_forward(q, k, v, o, lse, scale, causal, stream=None):
+    """fa_forward of include/fa.h on torch tensors; writes o and lse."""
+    B, Hq, Hkv, N, d = _shapes(q, k)
+    _bf16_cuda("q", q)
+    _bf16_cuda("k", k)
+    _bf16_cuda("v", v, k.shape)
+    _bf16_cuda("o", o, q.shape)
+    _f32_cuda("lse", lse, (B, Hq, N))
+    _check(library().fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), B, Hq, Hkv, N, d, ctypes.c_float(scale),
+                                int(bool(causal)), _stream(stream)), "fa_forward")
+
+
+def fa_backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, stream=None):
+    """fa_backward of include/fa.h on torch tensors; writes dq, dk, dv."""
+    B, Hq, Hkv, N, d = _shapes(q, k)
+    for name, t, shp in (("q", q, None), ("k", k, None), ("v", v, k.shape), ("o", o, q.shape),
+                         ("do", do, q.shape), ("dq", dq, q.shape), ("dk", dk, k.shape),
+                         ("dv", dv, k.shape)):
+        _bf16_cuda(name, t, shp)
+    _f32_cuda("lse", lse, (B, Hq, N))
+    _check(library().fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), B, Hq, Hkv, N, d, ctypes.c_float(scale),
+                                 int(bool(causal)), _stream(stream)), "fa_backward")
+
+
+def fa_backward_preprocess(o, do, D, stream=None):
+    """fa_backward_preprocess of include/fa.h: D[r] = sum_c dO[r, c] O[r, c]."""
+    _bf16_cuda("o", o)
+    _bf16_cuda("do", do, o.shape)
+    d = o.shape[-1]
+    rows = o.numel() // d
+    _f32_cuda("D", D, tuple(o.shape[:-1]))
+    _check(library().fa_backward_preprocess(o.data_ptr(), do.data_ptr(), D.data_ptr(), rows, d,
+                                            _stream(stream)), "fa_backward_preprocess")
+
+
+def fa_status_string(status):
+    return status_string(status)
+
+
+def fa_last_device_error(stream=None):
+    """Synchronises the stream; returns the status code (0 = FA_OK)."""
+    return int(library().fa_last_device_error(_stream(stream)))
+
+
+def fa_selftest_wait_timeout(limit_ms, stream=None):
+    _check(library().fa_selftest_wait_timeout(int(limit_ms), _stream(stream)),
+           "fa_selftest_wait_timeout")
+
+
+def attention_forward(q, k, v, causal=False, scale=None, stream=None):
+    """Allocates o and lse on q's device and runs fa_forward; returns (o, lse)."""
+    import torch
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    fa_forward(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, do, causal=False, scale=None, stream=None):
+    """Allocates dq, dk, dv on q's device and runs fa_backward; returns them."""
+    import torch
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    fa_backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, stream)
+    return dq, dk, dv

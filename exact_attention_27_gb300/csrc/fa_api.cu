@@ -1,0 +1,217 @@
+// C ABI of the exact-attention library (declared in include/fa.h): argument
+// validation, tensor-map encoding, dispatch to the kernels, error reporting.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace {
+
+// Bits set by kernels whose bounded waits ran out (one word per device).
+__device__ uint32_t g_fa_error_word;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Device address of g_fa_error_word on the current device, cached per device.
+uint32_t* error_word() {
+  static uint32_t* cache[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<uint32_t*>(p);
+  }
+  return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [planes][rows][cols] tensor seen as 3-D (cols, rows, planes) with a box of
+// box_cols x box_rows x 1.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr, int cols,
+              int rows, long long planes, int box_cols, int box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * elem_bytes,
+                           static_cast<cuuint64_t>(cols) * rows * elem_bytes};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long planes) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, d, N, planes, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+fa_status validate(int B, int H_q, int H_kv, int N, int d, float scale, int causal) {
+  if (B < 1 || H_q < 1 || H_kv < 1 || N < 1) return FA_ERR_INVALID_ARGUMENT;
+  if (H_q % H_kv != 0) return FA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARGUMENT;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARGUMENT;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const double elems = static_cast<double>(B) * H_q * N * d;
+  if (elems >= 1099511627776.0) return FA_ERR_INVALID_ARGUMENT;  // 2^40
+  if ((N + 127) / 128 > 65535) return FA_ERR_INVALID_ARGUMENT;   // grid.y limit
+  return FA_OK;
+}
+
+// A single thread waits on an mbarrier that nothing will ever complete, with
+// the caller's time limit, then records the timeout like the real kernels do.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = fa::smem_u32(&bar);
+  fa::mbar_init(b, 1);
+  fa::fence_barrier_init();
+  const uint64_t t0 = fa::globaltimer_ns();
+  while (!fa::mbar_try_wait(b, 0)) {
+    if (fa::globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(err, fa::kErrTimeoutOther);
+      return;
+    }
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H_q, int H_kv, int N, int d, float scale, int causal,
+                     cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARGUMENT;
+  const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_INVALID_ARGUMENT;
+  CUtensorMap tq, tk, tv;
+  if (!make_map_bf16(&tq, q, d, N, static_cast<long long>(B) * H_q) ||
+      !make_map_bf16(&tk, k, d, N, static_cast<long long>(B) * H_kv) ||
+      !make_map_bf16(&tv, v, d, N, static_cast<long long>(B) * H_kv))
+    return FA_ERR_CUDA;
+  uint32_t* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
+  return fa::launch_forward(tq, tk, tv, o, lse, s, err, stream) == cudaSuccess ? FA_OK
+                                                                               : FA_ERR_CUDA;
+}
+
+fa_status fa_backward_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
+                                 cudaStream_t stream) {
+  if (!o || !dO || !D || rows < 1) return FA_ERR_INVALID_ARGUMENT;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(o) || !aligned16(dO) || (reinterpret_cast<uintptr_t>(D) & 3u))
+    return FA_ERR_INVALID_ARGUMENT;
+  return fa::launch_preprocess(o, dO, D, rows, d, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                      int H_q, int H_kv, int N, int d, float scale, int causal,
+                      cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
+  const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
+  for (const void* p : p16)
+    if (!aligned16(p)) return FA_ERR_INVALID_ARGUMENT;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_INVALID_ARGUMENT;
+  uint32_t* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+
+  const long long rows = static_cast<long long>(B) * H_q * N;
+  const size_t d_bytes = static_cast<size_t>(rows) * sizeof(float);
+  const size_t acc_bytes = static_cast<size_t>(rows) * d * sizeof(float);
+  void* scratch = nullptr;
+  // D first, then the dQ accumulator (offset rounded up to 1 KB).
+  const size_t acc_off = (d_bytes + 1023) & ~static_cast<size_t>(1023);
+  if (cudaMallocAsync(&scratch, acc_off + acc_bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
+  float* Dbuf = static_cast<float*>(scratch);
+  float* acc = reinterpret_cast<float*>(static_cast<char*>(scratch) + acc_off);
+
+  fa::BwdMaps m;
+  bool ok = make_map_bf16(&m.q, q, d, N, static_cast<long long>(B) * H_q) &&
+            make_map_bf16(&m.k, k, d, N, static_cast<long long>(B) * H_kv) &&
+            make_map_bf16(&m.v, v, d, N, static_cast<long long>(B) * H_kv) &&
+            make_map_bf16(&m.dO, dO, d, N, static_cast<long long>(B) * H_q) &&
+            make_map(&m.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, d, N,
+                     static_cast<long long>(B) * H_q, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
+  cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
+  if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, acc_bytes, stream);
+  if (e == cudaSuccess) e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream);
+  if (e == cudaSuccess) e = fa::launch_backward(m, lse, Dbuf, acc, dk, dv, s, err, stream);
+  if (e == cudaSuccess) e = fa::launch_dq_finalize(acc, dq, rows * d, scale, stream);
+  const cudaError_t ef = cudaFreeAsync(scratch, stream);
+  return (e == cudaSuccess && ef == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension";
+    case FA_ERR_CUDA: return "CUDA runtime error";
+    case FA_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
+  }
+  return "unknown status";
+}
+
+fa_status fa_last_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  uint32_t* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, err, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (word == 0) return FA_OK;
+  if (cudaMemsetAsync(err, 0, sizeof(word), stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_ERR_DEVICE_TIMEOUT;
+}
+
+fa_status fa_selftest_wait_timeout(int limit_ms, cudaStream_t stream) {
+  if (limit_ms < 1 || limit_ms > 2000) return FA_ERR_INVALID_ARGUMENT;
+  uint32_t* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  wait_timeout_selftest_kernel<<<1, 1, 0, stream>>>(static_cast<uint64_t>(limit_ms) * 1000000ull,
+                                                    err);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,401 @@
+// Forward pass of exact attention on sm_103a.
+//
+// One CTA owns one tile of 128 query rows of one (batch, query head) and
+// streams the key/value tiles of its key/value head past it ("FlashAttention:
+// l'attenzione che non spreca memoria", section "L'idea: lavorare a tessere,
+// mai scrivere la matrice": the query block stays, K_j / V_j blocks move, the
+// S_ij tile is B_r x B_c, here 128 x 128).
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax: thread t owns query row t of the tile.  Online
+//              softmax per key tile, rescale of the O accumulator, epilogue.
+//   warp 4     TMA producer: Q once, then K_j and V_j into a ring of stages.
+//   warp 5     MMA issuer (one thread) and TMEM owner:
+//                S_j = Q K_j^T           (tcgen05.mma, A and B from shared memory)
+//                O  += P_j V_j           (tcgen05.mma, A = P from tensor memory)
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   columns   0..127  S buffer 0     (P_j as packed bf16 overwrites columns 0..63)
+//   columns 128..255  S buffer 1
+//   columns 256..256+D-1  O accumulator (fp32)
+// Two S buffers let the tensor core compute S_{j+1} while the softmax warps
+// work on S_j.
+//
+// Online softmax ("L'attention fusionnee", section "Le softmax en ligne"):
+// per key tile m' = max(m, max s), p = exp(s - m'), l = l e^(m - m') + sum p,
+// o = o e^(m - m') + p v, one division o / l after the last tile.  It runs in
+// the base-2 domain with scale * log2(e) folded into one multiply-add (the
+// exp2 form of "Flash Attention ... NVIDIA CUDA Tile", kernel interface
+// section).  The reference point m is moved only when the running maximum has
+// grown by more than kRescaleThreshold (in log2 units); otherwise the old m is
+// kept for both o and l, which leaves o / l unchanged and bounds every p by
+// 2^kRescaleThreshold.  The rescale of O then happens on few tiles.
+//
+// Causal masking ("L'attention fusionnee", same section: tiles that lie wholly
+// in the future are never visited; the mask is positional, no mask tensor):
+// query tile i visits key tiles 0..i only; the diagonal tile masks key > query.
+// Keys at or past N (ragged tail) are masked too.
+//
+// Every mbarrier wait is bounded (about a second); on expiry the kernel sets
+// an error bit, every role skips its remaining work and the CTA exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;                 // query rows per tile (MMA M)
+  static constexpr int BN = 128;                 // keys per tile (MMA N of Q K^T)
+  static constexpr int SUB = D / 64;             // 128-byte column blocks per row
+  static constexpr int SUB_BYTES = 128 * 128;    // one 128-row x 64-col bf16 block
+  static constexpr int TILE = SUB * SUB_BYTES;   // one 128 x D bf16 tile
+  static constexpr int NS = (D == 64) ? 4 : 2;   // K/V ring stages
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + TILE;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  // barrier slots
+  static constexpr int B_QFULL = 0;
+  static constexpr int B_KFULL = 1;
+  static constexpr int B_KEMPTY = B_KFULL + NS;
+  static constexpr int B_VFULL = B_KEMPTY + NS;
+  static constexpr int B_VEMPTY = B_VFULL + NS;
+  static constexpr int B_SFULL = B_VEMPTY + NS;  // 2
+  static constexpr int B_PFULL = B_SFULL + 2;    // 2
+  static constexpr int B_ODONE = B_PFULL + 2;
+  static constexpr int B_DRAIN = B_ODONE + 1;    // abort path: MMAs in flight
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort word
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_O = 256;
+};
+
+struct FwdParams {
+  __nv_bfloat16* o;
+  float* lse;
+  int N;
+  int Hq;
+  int G;          // query heads per key/value head
+  int n_qtiles;
+  int n_ktiles;
+  float scale_log2;  // scale * log2(e)
+  uint32_t* err;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int bh = blockIdx.x;  // flattened (batch, query head)
+  // Heaviest causal tiles are launched first.
+  const int qt = CAUSAL ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.y))
+                        : static_cast<int>(blockIdx.y);
+  const int b = bh / p.Hq;
+  const int hq = bh - b * p.Hq;
+  const int kvz = b * (p.Hq / p.G) + hq / p.G;  // flattened (batch, kv head)
+  const int n_kv = CAUSAL ? min(qt + 1, p.n_ktiles) : p.n_ktiles;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_QFULL), 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(bar(C::B_KFULL + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 1);
+      mbar_init(bar(C::B_VFULL + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_SFULL + s), 1);
+      mbar_init(bar(C::B_PFULL + s), 128);
+    }
+    mbar_init(bar(C::B_ODONE), 1);
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t sQ = sbase + C::OFF_Q;
+  const uint32_t sK = sbase + C::OFF_K;
+  const uint32_t sV = sbase + C::OFF_V;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t keep = policy_evict_last();  // K/V are re-read by the other query tiles
+      mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE);
+#pragma unroll
+      for (int s = 0; s < C::SUB; ++s)
+        tma_load_3d(sQ + s * C::SUB_BYTES, &tmQ, bar(C::B_QFULL), 64 * s, qt * C::BM, bh);
+      int issued = 0;  // K/V tiles whose loads were issued
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % C::NS;
+        const uint32_t ph = ((j / C::NS) - 1) & 1;
+        if (j >= C::NS &&
+            !mbar_wait(bar(C::B_KEMPTY + st), ph, abort_flag, p.err, kErrTimeoutLoad))
+          break;
+        mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE);
+#pragma unroll
+        for (int s = 0; s < C::SUB; ++s)
+          tma_load_3d_hint(sK + st * C::TILE + s * C::SUB_BYTES, &tmK, bar(C::B_KFULL + st),
+                           64 * s, j * C::BN, kvz, keep);
+        if (j >= C::NS &&
+            !mbar_wait(bar(C::B_VEMPTY + st), ph, abort_flag, p.err, kErrTimeoutLoad))
+          break;
+        mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE);
+#pragma unroll
+        for (int s = 0; s < C::SUB; ++s)
+          tma_load_3d_hint(sV + st * C::TILE + s * C::SUB_BYTES, &tmV, bar(C::B_VFULL + st),
+                           64 * s, j * C::BN, kvz, keep);
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        // Let the copies already issued land before the CTA's memory is released.
+        mbar_wait_timed(bar(C::B_QFULL), 0);
+        for (int j = max(0, issued - C::NS); j < issued; ++j) {
+          mbar_wait_timed(bar(C::B_KFULL + j % C::NS), (j / C::NS) & 1);
+          mbar_wait_timed(bar(C::B_VFULL + j % C::NS), (j / C::NS) & 1);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      bool ok = mbar_wait(bar(C::B_QFULL), 0, abort_flag, p.err, kErrTimeoutMma);
+      // S_j = Q K_j^T into S buffer j & 1; frees the K stage when done.
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % C::NS;
+        if (!mbar_wait(bar(C::B_KFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
+          return false;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+          mma_ss(d_tmem, smem_desc_sw128(sQ + off, 16, 1024),
+                 smem_desc_sw128(sK + st * C::TILE + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::B_SFULL + (j & 1)));
+        mma_commit(bar(C::B_KEMPTY + st));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (j + 1 < n_kv && !issue_s(j + 1)) break;
+        const int sb = j & 1;
+        const int st = j % C::NS;
+        if (!mbar_wait(bar(C::B_PFULL + sb), (j >> 1) & 1, abort_flag, p.err, kErrTimeoutMma))
+          break;
+        if (!mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // P occupies 64 packed columns; 16 keys = 8 columns per step.
+          // V block: 16 key rows of 128 bytes per step; D/64 blocks 16 KB apart.
+          mma_ts(tmem + C::COL_O, tmem + sb * 128 + kk * 8,
+                 smem_desc_sw128(sV + st * C::TILE + kk * 2048, C::SUB_BYTES, 1024), idesc_o,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(C::B_ODONE));
+        mma_commit(bar(C::B_VEMPTY + st));
+      }
+      if (*abort_flag) {
+        // Let the MMAs already issued finish before tensor memory is released.
+        mma_commit(bar(C::B_DRAIN));
+        mbar_wait_timed(bar(C::B_DRAIN), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (rows)
+    const int row = threadIdx.x;  // 0..127
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int qi = qt * C::BM + row;
+    const float c = p.scale_log2;
+    float m_used = -INFINITY;  // reference maximum, log2 domain
+    float l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int sb = j & 1;
+      // Waits are made warp-uniform: the TMEM loads and stores below are
+      // warp-collective, so either every lane goes on or every lane stops.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + sb), (j >> 1) & 1, abort_flag,
+                                             p.err, kErrTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          tmem_ld32(tmem + lane_off + sb * 128 + q4 * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) s[q4 * 32 + t] = __uint_as_float(r[t]);
+        }
+      }
+      const int kbase = j * C::BN;
+      const bool need_mask = CAUSAL ? (j == qt || kbase + C::BN > p.N) : (kbase + C::BN > p.N);
+      if (need_mask) {
+#pragma unroll
+        for (int t = 0; t < 128; ++t) {
+          const int key = kbase + t;
+          if (key >= p.N || (CAUSAL && key > qi)) s[t] = -INFINITY;
+        }
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int t = 1; t < 128; ++t) mx = fmaxf(mx, s[t]);
+      const float m_new = fmaxf(m_used, mx * c);
+      float alpha = 1.0f;
+      const bool upd = m_new > m_used + kRescaleThreshold;
+      if (upd) {
+        alpha = ex2_approx(m_used - m_new);
+        m_used = m_new;
+      }
+      const float m_ref = (m_used == -INFINITY) ? 0.0f : m_used;
+      float sum = 0.0f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * t], c, -m_ref));
+          const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * t + 1], c, -m_ref));
+          sum += p0 + p1;
+          pk[t] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tmem + lane_off + sb * 128 + h * 32, pk);
+      }
+      l = l * alpha + sum;
+      if (j > 0) {
+        // O holds P_0..P_{j-1} contributions; it must be final before rescaling.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE), (j - 1) & 1, abort_flag, p.err,
+                                               kErrTimeoutSoftmax));
+        if (!ok) break;
+        if (__any_sync(0xffffffffu, upd)) {
+          tc_fence_after();
+#pragma unroll
+          for (int q4 = 0; q4 < D / 32; ++q4) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + C::COL_O + q4 * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
+            tmem_st32(tmem + lane_off + C::COL_O + q4 * 32, r);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PFULL + sb));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE), (n_kv - 1) & 1, abort_flag,
+                                                   p.err, kErrTimeoutEpilogue));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const bool live = qi < p.N;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + (live ? qi : 0)) * D;
+#pragma unroll
+      for (int q4 = 0; q4 < D / 32; ++q4) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::COL_O + q4 * 32, r);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+          pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * inv_l,
+                              __uint_as_float(r[2 * t + 1]) * inv_l);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+        }
+      }
+      if (live) p.lse[static_cast<size_t>(bh) * p.N + qi] = (m_used + log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         void* o, float* lse, const AttnShape& s, uint32_t* err,
+                         cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  FwdParams p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.N = s.N;
+  p.Hq = s.Hq;
+  p.G = s.Hq / s.Hkv;
+  p.n_qtiles = (s.N + C::BM - 1) / C::BM;
+  p.n_ktiles = (s.N + C::BN - 1) / C::BN;
+  p.scale_log2 = s.scale * kLog2e;
+  p.err = err;
+  dim3 grid(static_cast<unsigned>(s.B * s.Hq), static_cast<unsigned>(p.n_qtiles));
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           void* o, float* lse, const AttnShape& s, uint32_t* err,
+                           cudaStream_t stream) {
+  if (s.d == 64)
+    return s.causal ? launch_fwd_t<64, true>(tq, tk, tv, o, lse, s, err, stream)
+                    : launch_fwd_t<64, false>(tq, tk, tv, o, lse, s, err, stream);
+  return s.causal ? launch_fwd_t<128, true>(tq, tk, tv, o, lse, s, err, stream)
+                  : launch_fwd_t<128, false>(tq, tk, tv, o, lse, s, err, stream);
+}
+
+}  // namespace fa

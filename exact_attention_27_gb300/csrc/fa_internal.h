@@ -1,0 +1,40 @@
+// Internal interface between the C-ABI layer (fa_api.cu) and the kernel
+// translation units.  Not installed; the public interface is include/fa.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fa {
+
+struct AttnShape {
+  int B, Hq, Hkv, N, d;
+  float scale;
+  int causal;
+};
+
+// Forward: q/k/v tensor maps (3-D: d, N, B*H; box 64 x 128 x 1; 128-byte
+// swizzle), outputs o (bf16) and lse (fp32).  Returns the launch status.
+cudaError_t launch_forward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           void* o, float* lse, const AttnShape& s, uint32_t* err,
+                           cudaStream_t stream);
+
+// Backward pass kernels (see fa_bwd.cu).
+cudaError_t launch_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
+                              cudaStream_t stream);
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dO;  // bf16, box 64 x 128 x 1, 128-byte swizzle
+  CUtensorMap dq_acc;       // fp32 accumulator, box 32 x 128 x 1, no swizzle
+};
+
+cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* D, float* dq_acc,
+                            void* dk, void* dv, const AttnShape& s, uint32_t* err,
+                            cudaStream_t stream);
+
+cudaError_t launch_dq_finalize(const float* dq_acc, void* dq, long long n, float scale,
+                               cudaStream_t stream);
+
+}  // namespace fa

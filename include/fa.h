@@ -1,0 +1,144 @@
+/*
+ * fa.h - C ABI of the exact-attention library for NVIDIA GB300 (sm_103a).
+ *
+ * Exact scaled-dot-product attention,
+ *     O = softmax(Q K^T * scale + causal mask) V,
+ * computed tile by tile with the online softmax so that the N x N scores S and
+ * weights P never reach device memory ("FlashAttention: l'attenzione che non
+ * spreca memoria", sections "L'idea: lavorare a tessere, mai scrivere la
+ * matrice" and "La online softmax, con i numeri"; "L'attention fusionnee",
+ * section "Le softmax en ligne").
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are contiguous, row-major, laid out [B][H][N][d] (batch, head,
+ *     position, head dimension), the (batch, heads, N, d_k) layout of the
+ *     PyTorch call in "FlashAttention: l'attenzione che non spreca memoria",
+ *     section "Cosa si guadagna (e cosa costa)".  Q, O, dO, dQ carry H_q heads;
+ *     K, V, dK, dV carry H_kv heads.  Query head h reads key/value head
+ *     h / (H_q / H_kv): contiguous groups, the QUERY_GROUP_SIZE of the CUDA
+ *     Tile kernel signature ("Flash Attention ... NVIDIA CUDA Tile",
+ *     section "Definiendo la interfaz del kernel").
+ *   - q, k, v, o, dO, dq, dk, dv hold bf16 values (IEEE binary16 with an 8-bit
+ *     exponent, "bfloat16"); lse holds fp32.  All arithmetic accumulates in
+ *     fp32; outputs are rounded to bf16 once, round-to-nearest-even.
+ *   - All pointers are DEVICE pointers on the current CUDA device.  The
+ *     caller allocates and owns every buffer; the library never frees or
+ *     retains them.  Each of q, k, v, o, dO, dq, dk, dv must be 16-byte
+ *     aligned (tensor-memory-accelerator copies); lse 4-byte aligned.
+ *   - causal = 1 applies the positional mask: query i sees keys j <= i
+ *     ("Flash Attention ... NVIDIA CUDA Tile", section "Atencion causal":
+ *     mask 0 where i >= j, -inf where i < j).  causal = 0: no mask.
+ *   - scale multiplies Q K^T; it must be finite and > 0 (1/sqrt(d) is usual).
+ *   - Work is enqueued on `stream` and the call returns without waiting.  A
+ *     fault inside a kernel surfaces at the caller's next synchronisation;
+ *     fa_last_device_error reports a timed-out wait inside a kernel.
+ *   - Nothing is printed and nothing aborts.
+ *
+ * Supported sizes: d in {64, 128}; B, H_q, H_kv, N >= 1; H_q % H_kv == 0;
+ * B * H_q * N * d < 2^40.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad size, bad scale */
+  FA_ERR_UNSUPPORTED = 2,      /* d not in {64, 128} */
+  FA_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed */
+  FA_ERR_DEVICE_TIMEOUT = 4    /* a bounded wait inside a kernel ran out */
+} fa_status;
+
+/*
+ * Forward pass.  Source: "L'attention fusionnee", section "Le softmax en
+ * ligne" (per key tile: m' = max(m, max s); p = exp(s - m');
+ * l = l e^(m - m') + sum p; o = o e^(m - m') + p v; one division o / l at the
+ * end) and section "La passe arriere : recalculer plutot que garder" (the forward
+ * stores L = m + ln l).
+ *
+ *   q   [B][H_q][N][d]   bf16, read
+ *   k   [B][H_kv][N][d]  bf16, read
+ *   v   [B][H_kv][N][d]  bf16, read
+ *   o   [B][H_q][N][d]   bf16, written: softmax(q k^T scale + mask) v
+ *   lse [B][H_q][N]      fp32, written: natural log of sum_j exp(scale q.k_j)
+ *                        over the keys the row sees (the scaled-score domain)
+ *
+ * Returns FA_OK once the work is enqueued; FA_ERR_INVALID_ARGUMENT or
+ * FA_ERR_UNSUPPORTED before any launch; FA_ERR_CUDA if the launch failed.
+ */
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H_q, int H_kv, int N, int d, float scale, int causal,
+                     cudaStream_t stream);
+
+/*
+ * Backward pass.  Source: "L'attention fusionnee", section "La passe
+ * arriere : recalculer plutot que garder": P is rebuilt tile by tile from the saved L as p = exp(s - L);
+ *   dV = P^T dO;  dS = P o (dO V^T - D) with D = rowsum(dO o O);
+ *   dQ = dS K scale;  dK = dS^T Q scale.
+ * D is computed by a reduction kernel before everything else (same section).
+ * For grouped-query attention, dK and dV of a shared head are the sums over
+ * the query heads that read it.
+ *
+ *   q, k, v, o, lse  as produced for / by fa_forward with the same sizes
+ *   dO  [B][H_q][N][d]   bf16, read: gradient of the loss w.r.t. o
+ *   dq  [B][H_q][N][d]   bf16, written
+ *   dk  [B][H_kv][N][d]  bf16, written
+ *   dv  [B][H_kv][N][d]  bf16, written
+ *
+ * Scratch: B*H_q*N*4 bytes for D and B*H_q*N*d*4 bytes for an fp32 dQ
+ * accumulator are taken stream-ordered (cudaMallocAsync on `stream`) and
+ * released the same way before the call returns; the caller's buffers are
+ * not used as scratch.  dq/dk/dv must not alias any input.
+ *
+ * Returns as fa_forward; FA_ERR_CUDA also when the scratch allocation fails.
+ */
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                      int H_q, int H_kv, int N, int d, float scale, int causal,
+                      cudaStream_t stream);
+
+/*
+ * The backward pass's first step on its own: D[r] = sum_c dO[r][c] * O[r][c]
+ * for every row r of [rows][d] bf16 matrices, accumulated in fp32 ("L'attention
+ * fusionnee", section "La passe arriere : recalculer plutot que garder": the sum of dP x P over a row of P
+ * equals the sum of dO x O over the row, one value per row).
+ *
+ *   o, dO  [rows][d] bf16 device pointers, 16-byte aligned, read
+ *   D      [rows]    fp32 device pointer, written
+ * d in {64, 128}; rows >= 1.  Same return codes as fa_forward.
+ */
+fa_status fa_backward_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
+                                 cudaStream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Synchronises `stream`, then reports what the kernels left behind: FA_ERR_CUDA
+ * for a pending CUDA error, FA_ERR_DEVICE_TIMEOUT if a bounded wait inside a
+ * kernel of this library ran out since the last call (the flag is then
+ * cleared), FA_OK otherwise.  Every wait inside the kernels gives up after
+ * about a second instead of hanging; the kernel then skips its remaining work.
+ */
+fa_status fa_last_device_error(cudaStream_t stream);
+
+/*
+ * Diagnostics for the bounded-wait error path (the pages have no counterpart):
+ * launches one thread that waits on a barrier nothing completes, gives up
+ * after `limit_ms` milliseconds (1..2000) and records a timeout exactly as the
+ * attention kernels do, so that a caller can check that fa_last_device_error
+ * reports FA_ERR_DEVICE_TIMEOUT and that the device stays usable.  Returns
+ * FA_OK once enqueued, FA_ERR_INVALID_ARGUMENT for a limit out of range.
+ */
+fa_status fa_selftest_wait_timeout(int limit_ms, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */
