@@ -167,7 +167,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
             make_map_bf16(&m.v, v, d, N, static_cast<long long>(B) * H_kv) &&
             make_map_bf16(&m.dO, dO, d, N, static_cast<long long>(B) * H_q) &&
             make_map(&m.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, d, N,
-                     static_cast<long long>(B) * H_q, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+                     static_cast<long long>(B) * H_q, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
   cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
   if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, acc_bytes, stream);

@@ -16,6 +16,8 @@
 namespace fa {
 namespace {
 
+constexpr float kLog2e = 1.4426950408889634f;
+
 // ------------------------------------------------------------------ B1
 // D / 8 threads per row, each loading 16 bytes of O and 16 bytes of dO;
 // the partial sums of a row are combined with warp shuffles.
@@ -58,6 +60,395 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float4* __restri
                      pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
 }
 
+
+// ------------------------------------------------------------------ B2
+//
+// One CTA owns one tile of 128 keys of one (batch, key/value head) and keeps
+// its dK and dV accumulators in tensor memory while it walks every query
+// tile of every query head of the group that sees those keys (FlashAttention-2
+// order as "L'attention fusionnee" describes it: one block per key tile,
+// dK and dV kept on chip, dQ added to global memory).  Keys sit on the 128
+// TMEM lanes, so each softmax thread owns one key row.  Per query tile i:
+//
+//   S^T  = K_j Q_i^T                  tcgen05.mma, A and B K-major in smem
+//   dP^T = V_j dO_i^T                 tcgen05.mma
+//   P^T  = exp2(S^T scale log2e - L_i log2e)      threads, L_i saved by the forward
+//   dS^T = P^T o (dP^T - D_i)                     threads, D_i from B1
+//   dV  += P^T dO_i                   tcgen05.mma, A = P^T (bf16) from TMEM
+//   dK  += dS^T Q_i                   tcgen05.mma, A = dS^T (bf16, K-major smem)
+//   dQ_i = dS K_j                     tcgen05.mma, A = the same dS^T buffer read
+//                                     MN-major; drained by a TMA reduce-add
+//                                     into the fp32 dQ accumulator
+// dK is multiplied by scale once at the end; dQ gets its scale in B3.
+//
+// Warp roles (192 threads): warps 0-3 key rows, warp 4 TMA, warp 5 MMA.
+// Tensor memory: dK [0, D), dV [D, 2D), S^T/P^T 128 columns, dP^T 128 columns,
+// dQ 64 columns after dP^T when D = 64, or in dP^T's columns when D = 128.
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BK = 128;                // keys per CTA
+  static constexpr int BQ = 128;                // queries per step
+  static constexpr int SUB = D / 64;
+  static constexpr int SUB_BYTES = 128 * 128;
+  static constexpr int TILE = SUB * SUB_BYTES;  // 128 x D bf16
+  static constexpr int NSQ = (D == 64) ? 2 : 1; // Q / dO stages
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;
+  static constexpr int OFF_DO = OFF_Q + NSQ * TILE;
+  static constexpr int OFF_DS = OFF_DO + NSQ * TILE;  // dS^T: 128 keys x 128 queries bf16
+  static constexpr int OFF_STG = OFF_DS + 2 * SUB_BYTES;  // dQ staging: 2 boxes 128 x 32 fp32
+  static constexpr int OFF_LD = OFF_STG + 2 * SUB_BYTES;  // L log2e [2][128], D [2][128]
+  static constexpr int OFF_BAR = OFF_LD + 4 * 128 * 4;
+  static constexpr int B_KV = 0;
+  static constexpr int B_QDFULL = 1;
+  static constexpr int B_QDEMPTY = B_QDFULL + NSQ;
+  static constexpr int B_SDP = B_QDEMPTY + NSQ;   // S^T and dP^T in TMEM
+  static constexpr int B_PDS = B_SDP + 1;         // P^T in TMEM and dS^T in smem (128 arrivals)
+  static constexpr int B_DQFULL = B_PDS + 1;      // dQ in TMEM, all MMAs of the step done
+  static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ columns drained (128 arrivals)
+  static constexpr int B_WG = B_DQFREE + 1;       // warpgroup-internal sync (128 arrivals)
+  static constexpr int B_DRAIN = B_WG + 1;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_DK = 0;
+  static constexpr uint32_t COL_DV = D;
+  static constexpr uint32_t COL_S = 2 * D;
+  static constexpr uint32_t COL_DP = 2 * D + 128;
+  static constexpr uint32_t COL_DQ = (D == 64) ? 2 * D + 256 : COL_DP;
+};
+
+struct BwdParams {
+  const float* lse;
+  const float* Dvec;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int N, Hq, Hkv, G, n_qtiles;
+  float scale;
+  float scale_log2;
+  uint32_t* err;
+};
+
+// Byte offset of 16-byte chunk `ch` of row `r` in a 128-byte-swizzled block
+// of 128-byte rows (the layout TMA and tcgen05 agree on).
+__device__ __forceinline__ uint32_t sw128(int r, int ch) {
+  return static_cast<uint32_t>(r * 128 + ((ch ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  float* sL = reinterpret_cast<float*>(smem + C::OFF_LD);        // [2][128]
+  float* sD = reinterpret_cast<float*>(smem + C::OFF_LD + 1024);  // [2][128]
+
+  const int warp = threadIdx.x >> 5;
+  const int kvz = blockIdx.x;  // flattened (batch, kv head)
+  const int jt = blockIdx.y;   // key tile
+  const int b = kvz / p.Hkv;
+  const int hkv = kvz - b * p.Hkv;
+  const int i0 = CAUSAL ? jt : 0;  // first query tile that sees this key tile
+  const int per_head = p.n_qtiles - i0;
+  const int n_steps = p.G * per_head;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_KV), 1);
+    for (int s = 0; s < C::NSQ; ++s) {
+      mbar_init(bar(C::B_QDFULL + s), 1);
+      mbar_init(bar(C::B_QDEMPTY + s), 1);
+    }
+    mbar_init(bar(C::B_SDP), 1);
+    mbar_init(bar(C::B_PDS), 128);
+    mbar_init(bar(C::B_DQFULL), 1);
+    mbar_init(bar(C::B_DQFREE), 128);
+    mbar_init(bar(C::B_WG), 128);
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t sK = sbase + C::OFF_K;
+  const uint32_t sV = sbase + C::OFF_V;
+  const uint32_t sQ = sbase + C::OFF_Q;
+  const uint32_t sdO = sbase + C::OFF_DO;
+  const uint32_t sDS = sbase + C::OFF_DS;
+  const uint32_t sSTG = sbase + C::OFF_STG;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE);
+#pragma unroll
+      for (int s = 0; s < C::SUB; ++s) {
+        tma_load_3d(sK + s * C::SUB_BYTES, &tmK, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
+        tma_load_3d(sV + s * C::SUB_BYTES, &tmV, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
+      }
+      int issued = 0;
+      for (int st_i = 0; st_i < n_steps; ++st_i) {
+        const int st = st_i % C::NSQ;
+        if (st_i >= C::NSQ && !mbar_wait(bar(C::B_QDEMPTY + st), ((st_i / C::NSQ) - 1) & 1,
+                                         abort_flag, p.err, kErrTimeoutLoad))
+          break;
+        const int g = st_i / per_head;
+        const int it = i0 + (st_i - g * per_head);
+        const int bhq = b * p.Hq + hkv * p.G + g;
+        mbar_arrive_expect_tx(bar(C::B_QDFULL + st), 2 * C::TILE);
+#pragma unroll
+        for (int s = 0; s < C::SUB; ++s) {
+          tma_load_3d(sQ + st * C::TILE + s * C::SUB_BYTES, &tmQ, bar(C::B_QDFULL + st), 64 * s,
+                      it * C::BQ, bhq);
+          tma_load_3d(sdO + st * C::TILE + s * C::SUB_BYTES, &tmdO, bar(C::B_QDFULL + st),
+                      64 * s, it * C::BQ, bhq);
+        }
+        issued = st_i + 1;
+      }
+      if (*abort_flag) {
+        mbar_wait_timed(bar(C::B_KV), 0);
+        for (int s2 = max(0, issued - C::NSQ); s2 < issued; ++s2)
+          mbar_wait_timed(bar(C::B_QDFULL + s2 % C::NSQ), (s2 / C::NSQ) & 1);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t id_kd = idesc_bf16_f32(128, D, false, true);     // dV, dK
+      constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);       // dQ
+      bool ok = mbar_wait(bar(C::B_KV), 0, abort_flag, p.err, kErrTimeoutMma);
+      for (int s = 0; ok && s < n_steps; ++s) {
+        const int st = s % C::NSQ;
+        const uint32_t q_st = sQ + st * C::TILE;
+        const uint32_t do_st = sdO + st * C::TILE;
+        if (!mbar_wait(bar(C::B_QDFULL + st), (s / C::NSQ) & 1, abort_flag, p.err,
+                       kErrTimeoutMma))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + C::COL_S, smem_desc_sw128(sK + off, 16, 1024),
+                 smem_desc_sw128(q_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
+        }
+        if (D == 128 && s > 0) {
+          // dQ of the previous step lives in dP^T's columns until drained.
+          if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + C::COL_DP, smem_desc_sw128(sV + off, 16, 1024),
+                 smem_desc_sw128(do_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::B_SDP));
+        if (!mbar_wait(bar(C::B_PDS), s & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+        tc_fence_after();
+        // dV += P^T dO_i   (A = P^T in TMEM: 16 queries = 8 packed columns per step)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8,
+                 smem_desc_sw128(do_st + kk * 2048, C::SUB_BYTES, 1024), id_kd,
+                 (s > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_i   (A = dS^T K-major: queries contiguous per key row)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + C::COL_DK, smem_desc_sw128(sDS + off, 16, 1024),
+                 smem_desc_sw128(q_st + kk * 2048, C::SUB_BYTES, 1024), id_kd,
+                 (s > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (D == 64 && s > 0) {
+          if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+          tc_fence_after();
+        }
+        // dQ_i = dS K_j    (A = dS: the dS^T buffer read MN-major; B = K_j MN-major)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::COL_DQ, smem_desc_sw128(sDS + kk * 2048, C::SUB_BYTES, 1024),
+                 smem_desc_sw128(sK + kk * 2048, C::SUB_BYTES, 1024), id_q, kk > 0 ? 1u : 0u);
+        mma_commit(bar(C::B_QDEMPTY + st));
+        mma_commit(bar(C::B_DQFULL));
+      }
+      if (*abort_flag) {
+        mma_commit(bar(C::B_DRAIN));
+        mbar_wait_timed(bar(C::B_DRAIN), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ key rows
+    const int t = threadIdx.x;  // key row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int key = jt * C::BK + t;
+    const bool key_live = key < p.N;
+    const float c = p.scale_log2;
+    uint32_t wg_phase = 0;
+    bool ok = true;
+    auto wg_sync = [&]() -> bool {
+      mbar_arrive(bar(C::B_WG));
+      const bool r = mbar_wait(bar(C::B_WG), wg_phase & 1, abort_flag, p.err, kErrTimeoutSoftmax);
+      ++wg_phase;
+      return __all_sync(0xffffffffu, r);
+    };
+    for (int s = 0; s < n_steps; ++s) {
+      const int g = s / per_head;
+      const int it = i0 + (s - g * per_head);
+      const int bhq = b * p.Hq + hkv * p.G + g;
+      const int q0 = it * C::BQ;
+      const int buf = s & 1;
+      {
+        const int qrow = q0 + t;
+        const bool live = qrow < p.N;
+        const size_t idx = static_cast<size_t>(bhq) * p.N + (live ? qrow : 0);
+        sL[buf * 128 + t] = live ? p.lse[idx] * kLog2e : INFINITY;  // dead rows: P = 0
+        sD[buf * 128 + t] = live ? p.Dvec[idx] : 0.0f;
+      }
+      if (!(ok = wg_sync())) break;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::B_SDP), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after();
+      const float* Lb = sL + buf * 128;
+      const float* Db = sD + buf * 128;
+      const bool diag = CAUSAL && (it == jt);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(tmem + lane_off + C::COL_S + cc * 32, sv);
+        tmem_ld32(tmem + lane_off + C::COL_DP + cc * 32, dpv);
+        tmem_wait_ld();
+        uint32_t pk[16], dk16[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int qq = cc * 32 + 2 * u + h;
+            float pr = ex2_approx(fmaf(__uint_as_float(sv[2 * u + h]), c, -Lb[qq]));
+            if (!key_live || (diag && key > q0 + qq)) pr = 0.0f;
+            pv[h] = pr;
+            dsv[h] = pr * (__uint_as_float(dpv[2 * u + h]) - Db[qq]);
+          }
+          pk[u] = pack_bf16x2(pv[0], pv[1]);
+          dk16[u] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        // P^T (bf16) over the S^T columns already read: queries cc*32.. -> columns cc*16..
+        tmem_st16(tmem + lane_off + C::COL_S + cc * 16, pk);
+        // dS^T row `t`, queries cc*32 .. cc*32+31: 4 chunks of 8 in block cc/2.
+        const uint32_t blk = sDS + (cc >> 1) * C::SUB_BYTES;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(blk + sw128(t, (cc & 1) * 4 + q4), dk16[4 * q4], dk16[4 * q4 + 1],
+                       dk16[4 * q4 + 2], dk16[4 * q4 + 3]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PDS));
+      // ---- drain dQ_i into the fp32 accumulator
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::B_DQFULL), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int pass = 0; pass < D / 64; ++pass) {
+        if (t == 0) bulk_wait_group_read0();  // staging free again
+        if (!(ok = wg_sync())) break;
+        uint32_t a[32], bb[32];
+        tmem_ld32(tmem + lane_off + C::COL_DQ + pass * 64, a);
+        tmem_ld32(tmem + lane_off + C::COL_DQ + pass * 64 + 32, bb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          st_shared_v4(sSTG + sw128(t, ch), a[4 * ch], a[4 * ch + 1], a[4 * ch + 2],
+                       a[4 * ch + 3]);
+          st_shared_v4(sSTG + C::SUB_BYTES + sw128(t, ch), bb[4 * ch], bb[4 * ch + 1],
+                       bb[4 * ch + 2], bb[4 * ch + 3]);
+        }
+        fence_proxy_async_smem();
+        if (!(ok = wg_sync())) break;
+        if (t == 0) {
+          tma_reduce_add_3d(&tmdQ, sSTG, pass * 64, q0, bhq);
+          tma_reduce_add_3d(&tmdQ, sSTG + C::SUB_BYTES, pass * 64 + 32, q0, bhq);
+          bulk_commit_group();
+        }
+      }
+      if (!ok) break;
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DQFREE));
+    }
+    if (t == 0) bulk_wait_group0();
+    // ---- epilogue: dK (times scale) and dV, one key row per thread
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* dk_row = p.dk + (static_cast<size_t>(kvz) * p.N + (key_live ? key : 0)) * D;
+      __nv_bfloat16* dv_row = p.dv + (static_cast<size_t>(kvz) * p.N + (key_live ? key : 0)) * D;
+#pragma unroll
+      for (int q4 = 0; q4 < D / 32; ++q4) {
+        uint32_t rk[32], rv[32];
+        tmem_ld32(tmem + lane_off + C::COL_DK + q4 * 32, rk);
+        tmem_ld32(tmem + lane_off + C::COL_DV + q4 * 32, rv);
+        tmem_wait_ld();
+        uint32_t pkk[16], pkv[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          pkk[u] = pack_bf16x2(__uint_as_float(rk[2 * u]) * p.scale,
+                               __uint_as_float(rk[2 * u + 1]) * p.scale);
+          pkv[u] = pack_bf16x2(__uint_as_float(rv[2 * u]), __uint_as_float(rv[2 * u + 1]));
+        }
+        if (key_live) {
+          uint4* dst_k = reinterpret_cast<uint4*>(dk_row + q4 * 32);
+          uint4* dst_v = reinterpret_cast<uint4*>(dv_row + q4 * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            dst_k[u] = make_uint4(pkk[4 * u], pkk[4 * u + 1], pkk[4 * u + 2], pkk[4 * u + 3]);
+            dst_v[u] = make_uint4(pkv[4 * u], pkv[4 * u + 1], pkv[4 * u + 2], pkv[4 * u + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_preprocess(const void* o, const void* dO, float* Dout, long long rows, int d,
@@ -84,9 +475,40 @@ cudaError_t launch_dq_finalize(const float* dq_acc, void* dq, long long n, float
   return cudaGetLastError();
 }
 
-cudaError_t launch_backward(const BwdMaps&, const float*, const float*, float*, void*, void*,
-                            const AttnShape&, uint32_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_t(const BwdMaps& m, const float* lse, const float* Dv, void* dk, void* dv,
+                         const AttnShape& s, uint32_t* err, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  auto kern = fa_bwd_kernel<D, CAUSAL>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  BwdParams p;
+  p.lse = lse;
+  p.Dvec = Dv;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.N = s.N;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.G = s.Hq / s.Hkv;
+  p.n_qtiles = (s.N + C::BQ - 1) / C::BQ;
+  p.scale = s.scale;
+  p.scale_log2 = s.scale * kLog2e;
+  p.err = err;
+  const int n_ktiles = (s.N + C::BK - 1) / C::BK;
+  dim3 grid(static_cast<unsigned>(s.B * s.Hkv), static_cast<unsigned>(n_ktiles));
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dO, m.dq_acc, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* Dv, float*, void* dk,
+                            void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream) {
+  if (s.d == 64)
+    return s.causal ? launch_bwd_t<64, true>(m, lse, Dv, dk, dv, s, err, stream)
+                    : launch_bwd_t<64, false>(m, lse, Dv, dk, dv, s, err, stream);
+  return s.causal ? launch_bwd_t<128, true>(m, lse, Dv, dk, dv, s, err, stream)
+                  : launch_bwd_t<128, false>(m, lse, Dv, dk, dv, s, err, stream);
 }
 
 }  // namespace fa

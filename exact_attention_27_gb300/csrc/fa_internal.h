@@ -27,7 +27,7 @@ cudaError_t launch_preprocess(const void* o, const void* dO, float* D, long long
 
 struct BwdMaps {
   CUtensorMap q, k, v, dO;  // bf16, box 64 x 128 x 1, 128-byte swizzle
-  CUtensorMap dq_acc;       // fp32 accumulator, box 32 x 128 x 1, no swizzle
+  CUtensorMap dq_acc;       // fp32 accumulator, box 32 x 128 x 1, 128-byte swizzle
 };
 
 cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* D, float* dq_acc,

@@ -45,6 +45,8 @@ def _declare(lib):
     lib.oracle_attention_backward.restype = ctypes.c_int
     lib.oracle_attention_backward.argtypes = [p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64,
                                               i64, dbl, ctypes.c_int, i64]
+    lib.oracle_row_dot.restype = ctypes.c_int
+    lib.oracle_row_dot.argtypes = [p, p, p, i64, i64]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -132,6 +134,23 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"oracle_attention_backward failed with code {rc}")
         return (dq, dk, dv, rowdot) if want_rowdot else (dq, dk, dv)
+
+
+    def row_dot(self, a, b):
+        """sum over the last axis of a * b, for arrays of equal shape [..., d]."""
+        a, b = _f64(a), _f64(b)
+        if a.shape != b.shape or a.ndim < 1:
+            raise ValueError("row_dot needs two arrays of equal shape")
+        out = np.zeros(a.shape[:-1])
+        rc = self.lib.oracle_row_dot(_ptr(a), _ptr(b), _ptr(out), a.size // a.shape[-1],
+                                     a.shape[-1])
+        if rc != 0:
+            raise RuntimeError(f"oracle_row_dot failed with code {rc}")
+        return out
+
+
+def row_dot(a, b):
+    return load().row_dot(a, b)
 
 
 def attention_forward(q, k, v, scale, causal, q_offset=0, rows=None):

@@ -269,3 +269,20 @@ int oracle_attention_backward(const double* q, const double* k, const double* v,
   }
   return status;
 }
+
+/*
+ * D[r] = sum_c a[r][c] * b[r][c] for `rows` rows of width d: the per-row
+ * quantity the fused backward computes first ("L'attention fusionnee",
+ * section "La passe arriere : recalculer plutot que garder": the sum of dP x P
+ * over a row equals the sum of dO x O, one value per row).
+ */
+int oracle_row_dot(const double* a, const double* b, double* out, int64_t rows, int64_t d) {
+  if (!a || !b || !out || rows < 0 || d < 1) return 1;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    double acc = 0.0;
+    for (int64_t c = 0; c < d; ++c) acc += a[r * d + c] * b[r * d + c];
+    out[r] = acc;
+  }
+  return 0;
+}

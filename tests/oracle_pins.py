@@ -314,7 +314,8 @@ def pin_delta_identity(orc):
     for causal in (False, True):
         o, _ = orc.forward(q, k, v, 0.5, causal)
         *_, rowdot = orc.backward(q, k, v, do, 0.5, causal, want_rowdot=True)
-        assert np.max(np.abs(rowdot - np.sum(do * o, axis=-1))) <= 1e-12
+        assert np.max(np.abs(rowdot - orc.row_dot(do, o))) <= 1e-12
+        assert np.max(np.abs(orc.row_dot(do, o) - np.einsum("bhnc,bhnc->bhn", do, o))) <= 1e-12
 
 
 def pin_gqa_gradient_is_group_sum(orc):

@@ -4,7 +4,11 @@ C-ABI binding, and comparisons against the CPU oracle.
 Tolerances (bf16 inputs, fp32 accumulation, bf16 outputs):
   O       max |err| <= 2e-2 and mean |err| <= 2e-3
   L       max |err| <= 1e-3
-  dQ/dK/dV  max |err| <= 5e-2 * max |reference|   (per tensor)
+  dQ/dK/dV  max |err| <= 5e-2 * max |reference|   (per tensor), and never
+           below 1e-4: where the exact gradient vanishes (one visible key, so
+           the softmax is constant) the relative bound would demand exact zeros,
+           while D = rowsum(dO o O) from the bf16 output and dP from the MMA
+           differ by fp32 rounding (about d * 2^-24 * |dO| |V|).
 """
 
 import numpy as np
@@ -17,6 +21,7 @@ O_MAX = 2e-2
 O_MEAN = 2e-3
 L_MAX = 1e-3
 GRAD_REL = 5e-2
+GRAD_ABS_FLOOR = 1e-4
 
 
 def gpu_forward(inp, causal, scale):
@@ -54,6 +59,6 @@ def check_grads(got, ref, what=""):
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         g = g.float().cpu().numpy().astype(np.float64)
         assert np.isfinite(g).all(), f"{what}: {name} not finite"
-        bound = GRAD_REL * np.abs(r).max()
+        bound = max(GRAD_REL * np.abs(r).max(), GRAD_ABS_FLOOR)
         err = np.abs(g - r).max()
         assert err <= bound, f"{what}: {name} max err {err:.3e} > {bound:.3e}"

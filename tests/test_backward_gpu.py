@@ -1,0 +1,103 @@
+"""Backward parity: dQ/dK/dV from the CUDA path (B1 preprocess, B2 main
+kernel, B3 finalise, through fa_backward) against the oracle's gradients
+computed with P materialised, on the same seeded bf16 inputs."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import check_forward, check_grads
+from workloads import WORKLOADS, as_f64, make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from exact_attention_27_gb300 import _build
+    _build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run_fwd_bwd(inp, causal, scale):
+    import exact_attention_27_gb300 as fa
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_forward(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == 0
+    return o, lse, (dq, dk, dv)
+
+
+def bwd_vs_oracle(inp, causal, scale):
+    o, lse, grads = run_fwd_bwd(inp, causal, scale)
+    f = {n: as_f64(inp[n]) for n in ("q", "k", "v", "do")}
+    o_ref, l_ref = oracle.attention_forward(f["q"], f["k"], f["v"], scale, causal)
+    check_forward(o, lse, o_ref, l_ref, "forward")
+    ref = oracle.attention_backward(f["q"], f["k"], f["v"], f["do"], scale, causal)
+    check_grads(grads, ref, "backward")
+    return grads
+
+
+def test_causal_train_n4096_d64():
+    w = WORKLOADS["causal_train_n4096_d64"]
+    bwd_vs_oracle(workload_inputs(w), w.causal, w.scale)
+
+
+@pytest.mark.parametrize("N", [1, 5, 70, 128, 129, 257, 600])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths(N, d, causal):
+    inp = make_inputs(1, 2, 2, N, d, seed=N * 3 + d, with_grad=True)
+    bwd_vs_oracle(inp, causal, 1.0 / math.sqrt(d))
+
+
+@pytest.mark.parametrize("G", [2, 4])
+@pytest.mark.parametrize("d", [64, 128])
+def test_grouped_query_heads(G, d):
+    """dK and dV of a shared head sum over the G query heads that read it."""
+    inp = make_inputs(2, 8, 8 // G, 300, d, seed=70 + G + d, with_grad=True)
+    bwd_vs_oracle(inp, True, 1.0 / math.sqrt(d))
+
+
+def test_d128_causal_mid_size():
+    inp = make_inputs(1, 4, 4, 1024, 128, seed=123, with_grad=True)
+    bwd_vs_oracle(inp, True, 1.0 / math.sqrt(128))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_preprocess_row_dot(d):
+    """B1 alone: D = rowsum(dO o O) against the oracle's row_dot."""
+    import exact_attention_27_gb300 as fa
+    inp = make_inputs(3, 5, 5, 333, d, seed=d, with_grad=True)
+    o, do = inp["q"].cuda(), inp["do"].cuda()
+    D = torch.empty(o.shape[:-1], dtype=torch.float32, device="cuda")
+    fa.fa_backward_preprocess(o, do, D)
+    torch.cuda.synchronize()
+    ref = oracle.row_dot(as_f64(inp["do"]), as_f64(inp["q"]))
+    mag = oracle.row_dot(np.abs(as_f64(inp["do"])), np.abs(as_f64(inp["q"])))
+    # products of bf16 values are exact in fp32; d additions in fp32
+    assert np.all(np.abs(D.cpu().numpy() - ref) <= d * 2.0 ** -24 * mag + 1e-6)
+
+
+def test_gradients_do_not_depend_on_output_buffers_contents():
+    """Outputs are fully written: garbage in dq/dk/dv beforehand changes nothing."""
+    import exact_attention_27_gb300 as fa
+    inp = make_inputs(1, 2, 1, 333, 64, seed=8, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_forward(q, k, v, causal=True)
+    outs = []
+    for fill in (0.0, float("nan")):
+        dq = torch.full_like(q, fill)
+        dk = torch.full_like(k, fill)
+        dv = torch.full_like(v, fill)
+        fa.fa_backward(q, k, v, o, lse, do, dq, dk, dv, 0.125, True)
+        torch.cuda.synchronize()
+        outs.append((dq.float(), dk.float(), dv.float()))
+    for a, b in zip(*outs):
+        assert torch.isfinite(b).all()
+        assert torch.allclose(a, b, atol=1e-2, rtol=0)

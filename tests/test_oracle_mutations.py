@@ -35,6 +35,8 @@ MUTATIONS = [
     ("bwd_dp_uses_keys",
      "const double* v_row = v_head + j * d;\n          double acc = 0.0;",
      "const double* v_row = k_head + j * d;\n          double acc = 0.0;"),
+    ("row_dot_wrong_operand", "acc += a[r * d + c] * b[r * d + c];",
+     "acc += a[r * d + c] * a[r * d + c];"),
     ("bwd_dq_uses_values",
      "const double* k_row = k_head + j * d;\n          for (int64_t c = 0; c < d; ++c) dq_row",
      "const double* k_row = v_head + j * d;\n          for (int64_t c = 0; c < d; ++c) dq_row"),
