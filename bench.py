@@ -1,0 +1,467 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch: fa_forward (S = QK^T,
+online softmax, O = PV, L) followed by fa_backward (D = rowsum(dO o O), the
+dK/dV/dQ kernel, dQ finalise), on the causal training workload
+B=2, H=8, N=4096, d=64 (bf16 in, fp32 accumulate).  FLOPs follow the usual
+convention: forward 4 B H N^2 d, backward 10 B H N^2 d (five products, the
+recompute included), both halved under the causal mask.
+
+Prints ONE JSON line (rank 0).  With --impl reference the same workload is
+timed on the host cores with the double-precision CPU oracle instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "attention TFLOP/s (causal bf16 fwd/bwd) and % of GB300 dense BF16 peak"
+STEP_WORKLOAD = "causal_train_n4096_d64"
+FWD_WORKLOADS = ["causal_n4096_d64", "causal_n8192_d128", "causal_gqa_n16384_d128"]
+FALLBACK_TFLOPS = 1900.0
+FALLBACK_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_TFLOPS, FALLBACK_GBS, "fallback"
+
+
+def kernel_traffic(kernel):
+    """Bytes per launch from the committed ncu summary, if the kernel's source
+    is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src_hash = source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel:
+            if parts[3] == src_hash:
+                return float(parts[2])
+    return None
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_27_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.15)
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world):
+    import torch
+    import exact_attention_27_gb300 as fa
+    from exact_attention_27_gb300 import _build
+
+    dev = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(_build.LIB_PATH):
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    w = WORKLOADS[STEP_WORKLOAD]
+    stream = torch.cuda.current_stream()
+    inp = make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, seed=rank * 100, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flops_fwd, flops_bwd = w.fwd_flops(), w.bwd_flops()
+
+    def step():
+        fa.fa_forward(q, k, v, o, lse, w.scale, True)
+        fa.fa_backward(q, k, v, o, lse, do, dq, dk, dv, w.scale, True)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_last_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for e in ev:  # create the events (torch creates them on first record)
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(K):
+            flush.fill_(float(i))  # L2 flush, outside the step's events
+            e = ev[i]
+            e[0].record(stream)
+            fa.fa_forward(q, k, v, o, lse, w.scale, True)
+            e[1].record(stream)
+            fa.fa_set_backward_events(e[2], e[3])
+            fa.fa_backward(q, k, v, o, lse, do, dq, dk, dv, w.scale, True)
+            e[4].record(stream)
+        fa.fa_set_backward_events(None, None)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    if fa.fa_last_device_error() != 0:
+        raise RuntimeError("device error during the timed steps")
+    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[4]) for e in ev]
+    bwd_main_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * (flops_fwd + flops_bwd) * K / (total_ms * 1e-3) / 1e12
+
+    tflops_peak, hbm_peak, peak_src = peaks()
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_main_avg = statistics.mean(bwd_main_ms)
+    if bwd_main_avg >= fwd_avg:
+        kname, kflops, kms = "fa_bwd_kernel<64,causal>", flops_bwd, bwd_main_avg
+    else:
+        kname, kflops, kms = "fa_fwd_kernel<64,causal>", flops_fwd, fwd_avg
+    achieved = kflops / (kms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1),
+                "peak": tflops_peak, "unit": "TFLOP/s", "frac": round(achieved / tflops_peak, 4),
+                "peak_source": f"{peak_src} bf16 burst",
+                "traffic": kernel_traffic(kname.split("<")[0] + "<64,causal>")}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.describe(), "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "N": w.N,
+                   "d": w.d, "causal": True, "step": "fa_forward + fa_backward",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed before every step (512 MiB write), flush outside the timing",
+                   "frac_of_peak": round(value / world / tflops_peak, 4)},
+        "fwd_ms": round(fwd_avg, 5), "bwd_ms": round(statistics.mean(bwd_ms), 5),
+        "bwd_main_kernel_ms": round(bwd_main_avg, 5),
+        "roofline": roofline,
+        "gpu_launches": 4 * K,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if rank == 0:
+        result["clocks"] = clocks.summary()
+        if not args.only_step:
+            result["fwd_workloads"] = forward_workloads(fa, torch, tflops_peak, peak_src)
+            result["e2e"] = end_to_end(fa, torch, w, min(K, 50))
+            if world == 1:
+                result["cpu_baseline"] = cpu_baseline(w)
+    return result
+
+
+def run_forward_only(args):
+    """fa_forward alone on one workload (used for kernel profiles)."""
+    import torch
+    import exact_attention_27_gb300 as fa
+    from exact_attention_27_gb300 import _build
+    _build.build()
+    w = WORKLOADS[args.forward_only]
+    inp = make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, seed=7)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
+    e.record()
+    torch.cuda.synchronize()
+    if fa.fa_last_device_error() != 0:
+        raise RuntimeError("device error")
+    ms = s.elapsed_time(e) / args.steps
+    return {"workload": w.describe(), "launches": args.warmup + args.steps, "ms": round(ms, 4),
+            "tflops": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1)}
+
+
+def forward_workloads(fa, torch, tflops_peak, peak_src):
+    """Forward-only throughput on the larger workloads (inputs larger than L2
+    for the d = 128 ones; L2 flushed before each launch for the smallest)."""
+    out = []
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for name in FWD_WORKLOADS:
+        w = WORKLOADS[name]
+        inp = make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, seed=7)
+        q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
+        reps = 20
+        times = []
+        for _ in range(reps):
+            flush.fill_(0.0)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
+            e.record()
+            times.append((s, e))
+        torch.cuda.synchronize()
+        ms = statistics.mean(s.elapsed_time(e) for s, e in times)
+        tf = w.fwd_flops() / (ms * 1e-3) / 1e12
+        out.append({"workload": w.describe(), "ms": round(ms, 4), "tflops": round(tf, 1),
+                    "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst"})
+        del q, k, v, o, lse, inp
+    torch.cuda.empty_cache()
+    return out
+
+
+def end_to_end(fa, torch, w, K):
+    """Same step through the public API with the inputs in pinned host memory:
+    host->device copies of q, k, v, dO and device->host reads of o, lse, dq,
+    dk, dv inside the timed region."""
+    inp = make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, seed=1, with_grad=True)
+    h = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+    d = {n: torch.empty_like(h[n], device="cuda") for n in h}
+    o = torch.empty_like(d["q"])
+    lse = torch.empty(d["q"].shape[:-1], dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+    outs_d = [o, lse, dq, dk, dv]
+    outs_h = [torch.empty_like(t, device="cpu").pin_memory() for t in outs_d]
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_d)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for n in h:
+            d[n].copy_(h[n], non_blocking=True)
+        fa.fa_forward(d["q"], d["k"], d["v"], o, lse, w.scale, True)
+        fa.fa_backward(d["q"], d["k"], d["v"], o, lse, d["do"], dq, dk, dv, w.scale, True)
+        for src, dst in zip(outs_d, outs_h):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    stream.synchronize()
+    total = 0.0
+    for _ in range(K):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        one()
+        e.record(stream)
+        e.synchronize()  # the host reads the step's results
+        total += s.elapsed_time(e)
+    ms = total / K
+    return {"value": round((w.fwd_flops() + w.bwd_flops()) / (ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ oracle arms
+
+def oracle_sample(w, q_block, step_index):
+    """Oracle forward + backward for one block of `q_block` query rows in every
+    head of the workload (full keys, causal), and the algorithmic FLOPs of the
+    rows processed.  Rows rotate through the sequence from step to step."""
+    import oracle
+
+    inp = _oracle_inputs(w)
+    nblk = w.N // q_block
+    r0 = (step_index * 7919 % nblk) * q_block
+    q = inp["q"][:, :, r0:r0 + q_block]
+    do = inp["do"][:, :, r0:r0 + q_block]
+    t0 = time.perf_counter()
+    oracle.attention_forward(q, inp["k"], inp["v"], w.scale, True, q_offset=r0)
+    oracle.attention_backward(q, inp["k"], inp["v"], do, w.scale, True, q_offset=r0)
+    dt = time.perf_counter() - t0
+    keys_seen = sum(i + 1 for i in range(r0, r0 + q_block))  # per head
+    heads = w.B * w.Hq
+    flops = heads * keys_seen * w.d * (4 + 10)
+    return flops, dt
+
+
+_INPUT_CACHE = {}
+
+
+def _oracle_inputs(w):
+    if w.name not in _INPUT_CACHE:
+        from workloads import as_f64
+        inp = make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, seed=0, with_grad=True)
+        _INPUT_CACHE[w.name] = {n: as_f64(t) for n, t in inp.items()}
+    return _INPUT_CACHE[w.name]
+
+
+def cpu_baseline(w):
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    workload: forward + backward of 256-row query blocks in all 16 heads."""
+    import oracle
+    q_block, flops, secs, steps = 256, 0.0, 0.0, 0
+    while secs < 10.0 and steps < 16:
+        f, dt = oracle_sample(w, q_block, steps)
+        flops += f
+        secs += dt
+        steps += 1
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s",
+            "cores": min(oracle.num_threads(), w.B * w.Hq), "kind": "oracle",
+            "sample": f"{steps} blocks of {q_block} query rows x {w.B * w.Hq} heads, "
+                      f"fwd+bwd against all {w.N} keys (causal), {secs:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The double-precision CPU oracle timed on the host cores, on the same
+    workload, metric and unit; each step a bounded sample of query rows."""
+    import oracle
+    w = WORKLOADS[STEP_WORKLOAD]
+    oracle.load()
+    # size the per-step sample so that warm-up + steps stay within ~2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    q_block = 256
+    f, dt = oracle_sample(w, q_block, 0)
+    while dt > budget and q_block > 16:
+        q_block //= 2
+        f, dt = oracle_sample(w, q_block, 0)
+    for i in range(args.warmup):
+        oracle_sample(w, q_block, i + 1)
+    flops, secs = 0.0, 0.0
+    for i in range(args.steps):
+        f, dt = oracle_sample(w, q_block, args.warmup + 1 + i)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    sample = (f"per step: {q_block} query rows x {w.B * w.Hq} heads, fwd+bwd against all "
+              f"{w.N} keys (causal)")
+    cores = min(oracle.num_threads(), w.B * w.Hq)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.describe(), "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "N": w.N,
+                   "d": w.d, "causal": True, "step": "oracle forward + backward"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only-step", action="store_true",
+                    help="time the step only (no extra workloads, e2e or CPU baseline)")
+    ap.add_argument("--forward-only", choices=sorted(WORKLOADS), default=None,
+                    help="run fa_forward alone on one workload (for kernel profiles)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.gpus != world and world > 1:
+        ap.error("--gpus must match the launcher's WORLD_SIZE")
+    if args.forward_only:
+        print(json.dumps(run_forward_only(args)), flush=True)
+        return
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -19,7 +19,7 @@ from ._lib import FaError, library, status_string  # noqa: F401
 
 __all__ = [
     "FaError", "fa_forward", "fa_backward", "fa_backward_preprocess", "fa_status_string",
-    "fa_last_device_error", "fa_selftest_wait_timeout", "attention_forward", "attention_backward",
+    "fa_last_device_error", "fa_selftest_wait_timeout", "fa_set_backward_events", "attention_forward", "attention_backward",
     "library",
 ]
 
@@ -119,6 +119,13 @@ def fa_last_device_error(stream=None):
 def fa_selftest_wait_timeout(limit_ms, stream=None):
     _check(library().fa_selftest_wait_timeout(int(limit_ms), _stream(stream)),
            "fa_selftest_wait_timeout")
+
+
+def fa_set_backward_events(before, after):
+    """Records torch.cuda.Event `before`/`after` around the backward main kernel
+    of later fa_backward calls (None, None switches the hook off)."""
+    h = (lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else None)
+    library().fa_set_backward_events(h(before), h(after))
 
 
 def attention_forward(q, k, v, causal=False, scale=None, stream=None):

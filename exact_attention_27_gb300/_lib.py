@@ -45,6 +45,8 @@ def _declare(lib):
     lib.fa_status_string.argtypes = [i]
     lib.fa_last_device_error.restype = i
     lib.fa_last_device_error.argtypes = [p]
+    lib.fa_set_backward_events.restype = None
+    lib.fa_set_backward_events.argtypes = [p, p]
     lib.fa_selftest_wait_timeout.restype = i
     lib.fa_selftest_wait_timeout.argtypes = [i, p]
     return lib

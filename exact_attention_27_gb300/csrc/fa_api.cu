@@ -17,6 +17,10 @@ namespace {
 // Bits set by kernels whose bounded waits ran out (one word per device).
 __device__ uint32_t g_fa_error_word;
 
+// Caller-owned events recorded around the backward main kernel (timing hook).
+cudaEvent_t g_bwd_before = nullptr;
+cudaEvent_t g_bwd_after = nullptr;
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -172,7 +176,10 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
   if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, acc_bytes, stream);
   if (e == cudaSuccess) e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream);
+  const bool timed = g_bwd_before && g_bwd_after;
+  if (e == cudaSuccess && timed) e = cudaEventRecord(g_bwd_before, stream);
   if (e == cudaSuccess) e = fa::launch_backward(m, lse, Dbuf, acc, dk, dv, s, err, stream);
+  if (e == cudaSuccess && timed) e = cudaEventRecord(g_bwd_after, stream);
   if (e == cudaSuccess) e = fa::launch_dq_finalize(acc, dq, rows * d, scale, stream);
   const cudaError_t ef = cudaFreeAsync(scratch, stream);
   return (e == cudaSuccess && ef == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
@@ -203,6 +210,11 @@ fa_status fa_last_device_error(cudaStream_t stream) {
       cudaStreamSynchronize(stream) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_ERR_DEVICE_TIMEOUT;
+}
+
+void fa_set_backward_events(cudaEvent_t before, cudaEvent_t after) {
+  g_bwd_before = before;
+  g_bwd_after = after;
 }
 
 fa_status fa_selftest_wait_timeout(int limit_ms, cudaStream_t stream) {

@@ -137,6 +137,17 @@ fa_status fa_last_device_error(cudaStream_t stream);
  */
 fa_status fa_selftest_wait_timeout(int limit_ms, cudaStream_t stream);
 
+/*
+ * Timing hook for the backward pass's main kernel (diagnostics; the pages have
+ * no counterpart).  When both events are non-NULL, every later fa_backward
+ * call records `before` on its stream immediately before launching the main
+ * dK/dV/dQ kernel and `after` immediately after it, so a caller can time that
+ * kernel alone with cudaEventElapsedTime.  Pass NULL, NULL to switch it off.
+ * The events are owned by the caller and must outlive their use.  The setting
+ * is process-wide and not synchronised: set it from one thread.
+ */
+void fa_set_backward_events(cudaEvent_t before, cudaEvent_t after);
+
 #ifdef __cplusplus
 }
 #endif
