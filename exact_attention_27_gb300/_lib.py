@@ -39,6 +39,8 @@ def _declare(lib):
     lib.fa_forward.argtypes = [p, p, p, p, p, i, i, i, i, i, f, i, p]
     lib.fa_backward.restype = i
     lib.fa_backward.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, p]
+    lib.fa_backward_noalloc.restype = i
+    lib.fa_backward_noalloc.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, p]
     lib.fa_backward_preprocess.restype = i
     lib.fa_backward_preprocess.argtypes = [p, p, p, ll, i, p]
     lib.fa_status_string.restype = ctypes.c_char_p

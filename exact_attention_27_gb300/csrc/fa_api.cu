@@ -109,6 +109,21 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, uint32_t* err) {
 
 }  // namespace
 
+namespace fa {
+
+uint32_t* device_error_word() { return error_word(); }
+
+bool encode_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long planes) {
+  return make_map_bf16(m, ptr, d, N, planes);
+}
+
+bool encode_map_f32_acc(CUtensorMap* m, const void* ptr, int d, int N, long long planes) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, d, N, planes, 32, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace fa
+
 extern "C" {
 
 fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -34,6 +34,13 @@ cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* D, 
                             void* dk, void* dv, const AttnShape& s, uint32_t* err,
                             cudaStream_t stream);
 
+// Helpers defined in fa_api.cu for other translation units: the per-device
+// error word the kernels' bounded waits report into, and tensor-map encoding
+// for bf16 [planes][N][d] tensors and the fp32 dQ accumulator.
+uint32_t* device_error_word();
+bool encode_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long planes);
+bool encode_map_f32_acc(CUtensorMap* m, const void* ptr, int d, int N, long long planes);
+
 cudaError_t launch_dq_finalize(const float* dq_acc, void* dq, long long n, float scale,
                                cudaStream_t stream);
 

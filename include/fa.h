@@ -103,6 +103,43 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       cudaStream_t stream);
 
 /*
+ * Scratch reserved by the library for fa_backward_noalloc, in bytes (32 MiB).
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * fa_backward without any device allocation (the paper has no counterpart).
+ *
+ * For callers that cannot allocate device memory at the point where they
+ * run the backward pass: for example an application whose device memory is
+ * already reserved by another allocator, or a plug-in that an inference or
+ * training engine calls at enqueue time under a no-allocation rule.  The
+ * arguments, layouts, results and return codes are those of fa_backward; the
+ * results agree with fa_backward's within rounding (dQ is summed in fp32 in
+ * an order that can differ between runs).
+ *
+ * Instead of the memory pool it uses a fixed array of FA_NOALLOC_SCRATCH_BYTES
+ * inside the library, reserved on every GPU that loads the library until the
+ * process exits.  It holds D and the fp32 dQ accumulator, so a call needs
+ *     ceil(B*H_q*N*4 / 1024)*1024 + B*H_q*N*d*4  bytes
+ * (for example B=2, H_q=8, N=4096, d=64: about 16.3 MiB); larger problems are
+ * rejected with FA_ERR_INVALID_ARGUMENT before anything is launched.
+ *
+ * The array is shared by all calls on a device and keeps the last call's
+ * contents; each call clears the part that must start at zero.  Calls whose
+ * work overlaps on the GPU (on different streams, or from several threads)
+ * race on that array: serialise them, e.g. by issuing them on one stream.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture begins.  No cudaMalloc, cudaFree or other
+ * allocating routine is called.
+ */
+fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                              int B, int H_q, int H_kv, int N, int d, float scale, int causal,
+                              cudaStream_t stream);
+
+/*
  * The backward pass's first step on its own: D[r] = sum_c dO[r][c] * O[r][c]
  * for every row r of [rows][d] bf16 matrices, accumulated in fp32 ("L'attention
  * fusionnee", section "La passe arriere : recalculer plutot que garder": the sum of dP x P over a row of P
