@@ -504,9 +504,7 @@ cudaError_t launch_bwd_t(const BwdMaps& m, const float* lse, const float* Dv, vo
 
 cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* Dv, float*, void* dk,
                             void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream) {
-  if (s.d == 64)
-    return s.causal ? launch_bwd_t<64, true>(m, lse, Dv, dk, dv, s, err, stream)
-                    : launch_bwd_t<64, false>(m, lse, Dv, dk, dv, s, err, stream);
+  if (s.d == 64) return launch_backward_d64(m, lse, Dv, dk, dv, s, err, stream);
   return s.causal ? launch_bwd_t<128, true>(m, lse, Dv, dk, dv, s, err, stream)
                   : launch_bwd_t<128, false>(m, lse, Dv, dk, dv, s, err, stream);
 }

@@ -1,0 +1,504 @@
+// Backward main kernel for head dimension 64 on sm_103a, pipelined.
+//
+// Same mathematics as the d = 128 kernel in fa_bwd.cu ("L'attention
+// fusionnee", section "La passe arriere : recalculer plutot que garder": P
+// rebuilt from L, dV = P^T dO, dS = P o (dP - D), dQ = dS K scale,
+// dK = dS^T Q scale), arranged so that the tensor core and the threads work
+// at the same time:
+//
+//  * One CTA owns 128 keys of one (batch, K/V head) and walks the query tiles
+//    of every query head of the group in halves of 64 queries ("half-steps").
+//  * K and V are copied once into tensor memory as bf16, so S^T = K Q^T and
+//    dP^T = V dO^T take their A operand from TMEM; P^T and dS^T are written
+//    back to TMEM as bf16, so dV += P^T dO and dK += dS^T Q do too.  Only
+//    dQ = dS K reads both operands from shared memory (dS^T read MN-major).
+//  * S^T/dP^T are double-buffered per half-step: while a warpgroup turns
+//    half h into P^T and dS^T, the tensor core finishes dV/dK of half h-1 and
+//    computes S^T/dP^T of half h+1.  Two warpgroups take alternate halves.
+//  * A third warpgroup copies K and V into TMEM, drains each query tile's dQ
+//    through a swizzled staging tile and a TMA reduce-add into the fp32
+//    accumulator, and writes dK (times scale) and dV at the end.
+//
+// Warps: 0-3 compute (even halves), 4-7 compute (odd halves), 8-11 dQ drain
+// and epilogue, 12 TMA producer, 13 MMA issuer.  448 threads, 1 CTA per SM.
+//
+// Tensor memory (512 columns):
+//   [  0, 64) dK      [ 64,128) dV      [128,160) K bf16   [160,192) V bf16
+//   [192,256) S^T buf0  [256,320) dP^T buf0  [320,384) S^T buf1  [384,448) dP^T buf1
+//   [448,512) dQ of the current query tile
+// P^T (bf16) overwrites the first 32 columns of its S^T buffer, dS^T (bf16)
+// the first 32 columns of its dP^T buffer.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Cfg64 {
+  static constexpr int BK = 128;                 // keys per CTA
+  static constexpr int BQ = 128;                 // queries per tile (two halves)
+  static constexpr int TILE = 128 * 128;         // 128 rows x 64 bf16
+  static constexpr int NSQ = 2;                  // Q / dO stages
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;
+  static constexpr int OFF_DO = OFF_Q + NSQ * TILE;
+  static constexpr int OFF_DS = OFF_DO + NSQ * TILE;  // 2 x (128 keys x 128 queries bf16)
+  static constexpr int DS_BYTES = 2 * TILE;
+  static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;  // dQ staging: 2 boxes 128 x 32 fp32
+  // per compute warpgroup, two slots (alternate half-steps): L[64], D[64]
+  static constexpr int OFF_LD = OFF_STG + 2 * TILE;
+  static constexpr int OFF_BAR = OFF_LD + 2 * 2 * 128 * 4;
+  // barriers
+  static constexpr int B_KV = 0;
+  static constexpr int B_KVT = 1;                 // K, V copied into TMEM (128 arrivals)
+  static constexpr int B_QDFULL = 2;              // [NSQ]
+  static constexpr int B_QDEMPTY = B_QDFULL + NSQ;
+  static constexpr int B_SDP = B_QDEMPTY + NSQ;   // [2] S^T/dP^T of a half ready
+  static constexpr int B_PDS = B_SDP + 2;         // [2] P^T/dS^T of a half ready (128 arrivals)
+  static constexpr int B_DSFREE = B_PDS + 2;      // [2] dS^T smem buffer of a tile free
+  static constexpr int B_DQFULL = B_DSFREE + 2;   // dQ of a tile in TMEM
+  static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ drained (128 arrivals)
+  static constexpr int B_WG = B_DQFREE + 1;       // [3] warpgroup-internal syncs (128 arrivals)
+  static constexpr int B_DRAIN = B_WG + 3;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int THREADS = 448;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_DK = 0, COL_DV = 64, COL_KT = 128, COL_VT = 160;
+  static constexpr uint32_t COL_BUF = 192;        // + 128 * buf: S^T, + 64: dP^T
+  static constexpr uint32_t COL_DQ = 448;
+};
+
+struct Params64 {
+  const float* lse;
+  const float* Dvec;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int N, Hq, Hkv, G, n_qtiles;
+  float scale;
+  float scale_log2;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ uint32_t sw128(int r, int ch) {
+  return static_cast<uint32_t>(r * 128 + ((ch ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(448, 1)
+    fa_bwd64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmdO,
+                    const __grid_constant__ CUtensorMap tmdQ, const Params64 p) {
+  using C = Cfg64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int wg = warp >> 2;  // 0, 1 compute; 2 drain; 3 = warps 12, 13
+  const int n_kv_units = gridDim.x / ((p.N + C::BK - 1) / C::BK);
+  // Heaviest key tiles (most query tiles under the causal mask) first.
+  const int jt = static_cast<int>(blockIdx.x) / n_kv_units;
+  const int kvz = static_cast<int>(blockIdx.x) - jt * n_kv_units;  // flattened (batch, kv head)
+  const int b = kvz / p.Hkv;
+  const int hkv = kvz - b * p.Hkv;
+  const int i0 = CAUSAL ? jt : 0;
+  const int per_head = p.n_qtiles - i0;
+  const int n_steps = p.G * per_head;
+  const int n_half = 2 * n_steps;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_KV), 1);
+    mbar_init(bar(C::B_KVT), 128);
+    for (int s = 0; s < C::NSQ; ++s) {
+      mbar_init(bar(C::B_QDFULL + s), 1);
+      mbar_init(bar(C::B_QDEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_SDP + s), 1);
+      mbar_init(bar(C::B_PDS + s), 128);
+      mbar_init(bar(C::B_DSFREE + s), 1);
+    }
+    mbar_init(bar(C::B_DQFULL), 1);
+    mbar_init(bar(C::B_DQFREE), 128);
+    for (int s = 0; s < 3; ++s) mbar_init(bar(C::B_WG + s), 128);
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t sK = sbase + C::OFF_K;
+  const uint32_t sV = sbase + C::OFF_V;
+  const uint32_t sQ = sbase + C::OFF_Q;
+  const uint32_t sdO = sbase + C::OFF_DO;
+  const uint32_t sDS = sbase + C::OFF_DS;
+  const uint32_t sSTG = sbase + C::OFF_STG;
+
+  // step -> (query head within the group, query tile)
+  auto step_coords = [&](int s, int& bhq, int& it) {
+    const int g = s / per_head;
+    it = i0 + (s - g * per_head);
+    bhq = b * p.Hq + hkv * p.G + g;
+  };
+
+  if (warp == 12) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE);
+      tma_load_3d(sK, &tmK, bar(C::B_KV), 0, jt * C::BK, kvz);
+      tma_load_3d(sV, &tmV, bar(C::B_KV), 0, jt * C::BK, kvz);
+      int issued = 0;
+      for (int s = 0; s < n_steps; ++s) {
+        const int st = s % C::NSQ;
+        if (s >= C::NSQ && !mbar_wait(bar(C::B_QDEMPTY + st), ((s / C::NSQ) - 1) & 1,
+                                      abort_flag, p.err, kErrTimeoutLoad))
+          break;
+        int bhq, it;
+        step_coords(s, bhq, it);
+        mbar_arrive_expect_tx(bar(C::B_QDFULL + st), 2 * C::TILE);
+        tma_load_3d(sQ + st * C::TILE, &tmQ, bar(C::B_QDFULL + st), 0, it * C::BQ, bhq);
+        tma_load_3d(sdO + st * C::TILE, &tmdO, bar(C::B_QDFULL + st), 0, it * C::BQ, bhq);
+        issued = s + 1;
+      }
+      if (*abort_flag) {
+        mbar_wait_timed(bar(C::B_KV), 0);
+        for (int s2 = max(0, issued - C::NSQ); s2 < issued; ++s2)
+          mbar_wait_timed(bar(C::B_QDFULL + s2 % C::NSQ), (s2 / C::NSQ) & 1);
+      }
+    }
+  } else if (warp == 13) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t id_sdp = idesc_bf16_f32(128, 64, false, false);  // S^T, dP^T
+      constexpr uint32_t id_kv = idesc_bf16_f32(128, 64, false, true);    // dV, dK
+      constexpr uint32_t id_q = idesc_bf16_f32(128, 64, true, true);      // dQ
+      bool ok = mbar_wait(bar(C::B_KVT), 0, abort_flag, p.err, kErrTimeoutMma);
+      // S^T and dP^T of half h into buffer h & 1.
+      auto issue_sdp = [&](int h) -> bool {
+        const int s = h >> 1, a = h & 1, st = s % C::NSQ;
+        if (a == 0 && !mbar_wait(bar(C::B_QDFULL + st), (s / C::NSQ) & 1, abort_flag, p.err,
+                                 kErrTimeoutMma))
+          return false;
+        tc_fence_after();
+        const uint32_t buf = tmem + C::COL_BUF + 128 * (h & 1);
+        const uint32_t q_half = sQ + st * C::TILE + a * 8192;
+        const uint32_t do_half = sdO + st * C::TILE + a * 8192;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(buf, tmem + C::COL_KT + kk * 8, smem_desc_sw128(q_half + kk * 32, 16, 1024),
+                 id_sdp, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(buf + 64, tmem + C::COL_VT + kk * 8, smem_desc_sw128(do_half + kk * 32, 16, 1024),
+                 id_sdp, kk > 0 ? 1u : 0u);
+        mma_commit(bar(C::B_SDP + (h & 1)));
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      if (ok && n_half > 1) ok = issue_sdp(1);
+      for (int h = 0; ok && h < n_half; ++h) {
+        const int s = h >> 1, a = h & 1, st = s % C::NSQ;
+        if (!mbar_wait(bar(C::B_PDS + a), (h >> 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+        tc_fence_after();
+        const uint32_t buf = tmem + C::COL_BUF + 128 * a;
+        const uint32_t q_half = sQ + st * C::TILE + a * 8192;
+        const uint32_t do_half = sdO + st * C::TILE + a * 8192;
+        // dV += P^T dO_h ; dK += dS^T Q_h  (64 queries = 4 steps of 16)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + C::COL_DV, buf + kk * 8, smem_desc_sw128(do_half + kk * 2048, 16384, 1024),
+                 id_kv, (h > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + C::COL_DK, buf + 64 + kk * 8,
+                 smem_desc_sw128(q_half + kk * 2048, 16384, 1024), id_kv,
+                 (h > 0 || kk > 0) ? 1u : 0u);
+        if (a == 1) {
+          if (s > 0) {
+            if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma))
+              break;
+            tc_fence_after();
+          }
+          // dQ = dS K_j: A = dS (query rows) read MN-major from the dS^T tile.
+          const uint32_t ds = sDS + (s & 1) * C::DS_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::COL_DQ, smem_desc_sw128(ds + kk * 2048, C::TILE, 1024),
+                   smem_desc_sw128(sK + kk * 2048, C::TILE, 1024), id_q, kk > 0 ? 1u : 0u);
+          mma_commit(bar(C::B_DQFULL));
+          mma_commit(bar(C::B_DSFREE + (s & 1)));
+          mma_commit(bar(C::B_QDEMPTY + st));
+        }
+        if (h + 2 < n_half && !issue_sdp(h + 2)) break;
+      }
+      if (*abort_flag) {
+        mma_commit(bar(C::B_DRAIN));
+        mbar_wait_timed(bar(C::B_DRAIN), 0);
+      }
+    }
+  } else if (wg < 2) {
+    // ------------------------------------------------------------ compute (key rows)
+    const int t = threadIdx.x & 127;  // key row
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int key = jt * C::BK + t;
+    const bool key_live = key < p.N;
+    const float c = p.scale_log2;
+    // L[64], D[64] of the current half; two slots so that a fast thread
+    // filling the next half cannot overwrite values a slow thread still reads
+    float* sLD0 = reinterpret_cast<float*>(smem + C::OFF_LD + wg * 1024);
+    uint32_t wg_phase = 0;
+    bool ok = true;
+    // prefetch of this warpgroup's first half: thread t < 64 loads L, t >= 64 loads D
+    auto fetch = [&](int h) -> float {
+      const int s = h >> 1;
+      int bhq, it;
+      step_coords(s, bhq, it);
+      const int qrow = it * C::BQ + (h & 1) * 64 + (t & 63);
+      if (qrow >= p.N) return t < 64 ? INFINITY : 0.0f;  // dead rows: P = 0
+      const size_t idx = static_cast<size_t>(bhq) * p.N + qrow;
+      return t < 64 ? p.lse[idx] * kLog2e : p.Dvec[idx];
+    };
+    float pre = (wg < n_half) ? fetch(wg) : 0.0f;
+    for (int h = wg; h < n_half; h += 2) {
+      const int s = h >> 1;
+      int bhq, it;
+      step_coords(s, bhq, it);
+      const int q0 = it * C::BQ + (h & 1) * 64;
+      float* sLD = sLD0 + ((h >> 1) & 1) * 128;
+      sLD[t] = pre;
+      if (h + 2 < n_half) pre = fetch(h + 2);
+      mbar_arrive(bar(C::B_WG + wg));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_WG + wg), wg_phase & 1, abort_flag, p.err,
+                                             kErrTimeoutSoftmax));
+      ++wg_phase;
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SDP + wg), (h >> 1) & 1, abort_flag,
+                                             p.err, kErrTimeoutSoftmax));
+      if (!ok) break;
+      if (s >= 2) {  // the dS^T buffer of tile s - 2 must have been read by its dQ MMA
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DSFREE + (s & 1)), ((s - 2) >> 1) & 1,
+                                               abort_flag, p.err, kErrTimeoutSoftmax));
+        if (!ok) break;
+      }
+      tc_fence_after();
+      const uint32_t buf = tmem + lane_off + C::COL_BUF + 128 * wg;
+      const bool diag = CAUSAL && (it == jt);
+      const uint32_t ds_blk = sDS + (s & 1) * C::DS_BYTES + wg * C::TILE;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(buf + cc * 32, sv);
+        tmem_ld32(buf + 64 + cc * 32, dpv);
+        tmem_wait_ld();
+        uint32_t pk[16], dk16[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int qq = cc * 32 + 2 * u + e;
+            float pr = ex2_approx(fmaf(__uint_as_float(sv[2 * u + e]), c, -sLD[qq]));
+            if (!key_live || (diag && key > q0 + qq)) pr = 0.0f;
+            pv[e] = pr;
+            dsv[e] = pr * (__uint_as_float(dpv[2 * u + e]) - sLD[64 + qq]);
+          }
+          pk[u] = pack_bf16x2(pv[0], pv[1]);
+          dk16[u] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        tmem_st16(buf + cc * 16, pk);          // P^T over S^T
+        tmem_st16(buf + 64 + cc * 16, dk16);   // dS^T over dP^T
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(ds_blk + sw128(t, cc * 4 + q4), dk16[4 * q4], dk16[4 * q4 + 1],
+                       dk16[4 * q4 + 2], dk16[4 * q4 + 3]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PDS + wg));
+    }
+  } else if (wg == 2) {
+    // ------------------------------------------------------------ K/V -> TMEM, dQ drain, epilogue
+    const int t = threadIdx.x & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t wg_phase = 0;
+    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KV), 0, abort_flag, p.err,
+                                                kErrTimeoutOther));
+    if (ok) {
+      // Row t of K and V (64 bf16 = 8 swizzled 16-byte chunks) -> 32 TMEM columns.
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t src = which == 0 ? sK : sV;
+        uint32_t r[32];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 v = ld_shared_v4(src + sw128(t, ch));
+          r[4 * ch] = v.x;
+          r[4 * ch + 1] = v.y;
+          r[4 * ch + 2] = v.z;
+          r[4 * ch + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + (which == 0 ? C::COL_KT : C::COL_VT), r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_KVT));
+    }
+    auto wg_sync = [&]() -> bool {
+      mbar_arrive(bar(C::B_WG + 2));
+      const bool r = mbar_wait(bar(C::B_WG + 2), wg_phase & 1, abort_flag, p.err, kErrTimeoutOther);
+      ++wg_phase;
+      return __all_sync(0xffffffffu, r);
+    };
+    for (int s = 0; ok && s < n_steps; ++s) {
+      int bhq, it;
+      step_coords(s, bhq, it);
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::B_DQFULL), s & 1, abort_flag, p.err, kErrTimeoutOther));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t a[32], bb[32];
+      tmem_ld32(tmem + lane_off + C::COL_DQ, a);
+      tmem_ld32(tmem + lane_off + C::COL_DQ + 32, bb);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DQFREE));  // dQ columns may be overwritten now
+      if (t == 0) bulk_wait_group_read0();  // staging free again
+      if (!(ok = wg_sync())) break;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        st_shared_v4(sSTG + sw128(t, ch), a[4 * ch], a[4 * ch + 1], a[4 * ch + 2], a[4 * ch + 3]);
+        st_shared_v4(sSTG + C::TILE + sw128(t, ch), bb[4 * ch], bb[4 * ch + 1], bb[4 * ch + 2],
+                     bb[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      if (!(ok = wg_sync())) break;
+      if (t == 0) {
+        tma_reduce_add_3d(&tmdQ, sSTG, 0, it * C::BQ, bhq);
+        tma_reduce_add_3d(&tmdQ, sSTG + C::TILE, 32, it * C::BQ, bhq);
+        bulk_commit_group();
+      }
+    }
+    if (t == 0) bulk_wait_group0();
+    // ---- epilogue: every MMA has completed once the last dQ was seen
+    if (ok) {
+      tc_fence_after();
+      const int key = jt * C::BK + t;
+      const bool live = key < p.N;
+      __nv_bfloat16* dk_row = p.dk + (static_cast<size_t>(kvz) * p.N + (live ? key : 0)) * 64;
+      __nv_bfloat16* dv_row = p.dv + (static_cast<size_t>(kvz) * p.N + (live ? key : 0)) * 64;
+#pragma unroll
+      for (int q4 = 0; q4 < 2; ++q4) {
+        uint32_t rk[32], rv[32];
+        tmem_ld32(tmem + lane_off + C::COL_DK + q4 * 32, rk);
+        tmem_ld32(tmem + lane_off + C::COL_DV + q4 * 32, rv);
+        tmem_wait_ld();
+        uint32_t pkk[16], pkv[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          pkk[u] = pack_bf16x2(__uint_as_float(rk[2 * u]) * p.scale,
+                               __uint_as_float(rk[2 * u + 1]) * p.scale);
+          pkv[u] = pack_bf16x2(__uint_as_float(rv[2 * u]), __uint_as_float(rv[2 * u + 1]));
+        }
+        if (live) {
+          uint4* dst_k = reinterpret_cast<uint4*>(dk_row + q4 * 32);
+          uint4* dst_v = reinterpret_cast<uint4*>(dv_row + q4 * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            dst_k[u] = make_uint4(pkk[4 * u], pkk[4 * u + 1], pkk[4 * u + 2], pkk[4 * u + 3]);
+            dst_v[u] = make_uint4(pkv[4 * u], pkv[4 * u + 1], pkv[4 * u + 2], pkv[4 * u + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <bool CAUSAL>
+cudaError_t launch_t(const BwdMaps& m, const float* lse, const float* Dv, void* dk, void* dv,
+                     const AttnShape& s, uint32_t* err, cudaStream_t stream) {
+  using C = Cfg64;
+  auto kern = fa_bwd64_kernel<CAUSAL>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  Params64 p;
+  p.lse = lse;
+  p.Dvec = Dv;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.N = s.N;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.G = s.Hq / s.Hkv;
+  p.n_qtiles = (s.N + C::BQ - 1) / C::BQ;
+  p.scale = s.scale;
+  p.scale_log2 = s.scale * kLog2e;
+  p.err = err;
+  const long long n_ktiles = (s.N + C::BK - 1) / C::BK;
+  const long long grid = n_ktiles * s.B * s.Hkv;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dO,
+                                                                         m.dq_acc, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward_d64(const BwdMaps& m, const float* lse, const float* Dv, void* dk,
+                                void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream) {
+  return s.causal ? launch_t<true>(m, lse, Dv, dk, dv, s, err, stream)
+                  : launch_t<false>(m, lse, Dv, dk, dv, s, err, stream);
+}
+
+}  // namespace fa

@@ -109,10 +109,12 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5;
-  const int bh = blockIdx.x;  // flattened (batch, query head)
-  // Heaviest causal tiles are launched first.
-  const int qt = CAUSAL ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.y))
-                        : static_cast<int>(blockIdx.y);
+  // Launch order: head-major, so the CTAs in flight at any time share the
+  // K/V of a few heads (which then stay in L2); within a head the heaviest
+  // causal tiles come first.
+  const int bh = static_cast<int>(blockIdx.x) / p.n_qtiles;  // flattened (batch, query head)
+  const int qi_ = static_cast<int>(blockIdx.x) - bh * p.n_qtiles;
+  const int qt = CAUSAL ? (p.n_qtiles - 1 - qi_) : qi_;
   const int b = bh / p.Hq;
   const int hq = bh - b * p.Hq;
   const int kvz = b * (p.Hq / p.G) + hq / p.G;  // flattened (batch, kv head)
@@ -381,8 +383,9 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   p.n_ktiles = (s.N + C::BN - 1) / C::BN;
   p.scale_log2 = s.scale * kLog2e;
   p.err = err;
-  dim3 grid(static_cast<unsigned>(s.B * s.Hq), static_cast<unsigned>(p.n_qtiles));
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  const long long grid = static_cast<long long>(s.B) * s.Hq * p.n_qtiles;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -30,6 +30,10 @@ struct BwdMaps {
   CUtensorMap dq_acc;       // fp32 accumulator, box 32 x 128 x 1, 128-byte swizzle
 };
 
+// Head dimension 64 (fa_bwd_d64.cu); launch_backward dispatches to it.
+cudaError_t launch_backward_d64(const BwdMaps& m, const float* lse, const float* D, void* dk,
+                                void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream);
+
 cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* D, float* dq_acc,
                             void* dk, void* dv, const AttnShape& s, uint32_t* err,
                             cudaStream_t stream);
