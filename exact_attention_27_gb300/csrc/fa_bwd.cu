@@ -409,6 +409,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(bar(C::B_DQFREE));
     }
     if (t == 0) bulk_wait_group0();
+    __syncwarp();  // lane 0 waited alone; the TMEM loads below are warp-collective
     // ---- epilogue: dK (times scale) and dV, one key row per thread
     if (ok) {
       tc_fence_after();
@@ -440,6 +441,9 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
+  // Every warp reconverges first: in the TMA and MMA warps only one lane did
+  // the work, and the CTA barrier below must count whole, converged warps.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {

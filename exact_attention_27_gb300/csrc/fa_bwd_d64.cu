@@ -12,22 +12,27 @@
 //    dP^T = V dO^T take their A operand from TMEM; P^T and dS^T are written
 //    back to TMEM as bf16, so dV += P^T dO and dK += dS^T Q do too.  Only
 //    dQ = dS K reads both operands from shared memory (dS^T read MN-major).
-//  * S^T/dP^T are double-buffered per half-step: while a warpgroup turns
-//    half h into P^T and dS^T, the tensor core finishes dV/dK of half h-1 and
-//    computes S^T/dP^T of half h+1.  Two warpgroups take alternate halves.
-//  * A third warpgroup copies K and V into TMEM, drains each query tile's dQ
-//    through a swizzled staging tile and a TMA reduce-add into the fp32
-//    accumulator, and writes dK (times scale) and dV at the end.
+//  * S^T/dP^T are double-buffered per half-step: while the threads turn half
+//    h into P^T and dS^T, the tensor core finishes dV/dK of half h-1 and
+//    computes S^T/dP^T of half h+1.  Both compute warpgroups work on every
+//    half, each on 32 of its 64 query columns, which halves the dependent
+//    chain each warp runs per half (the work there is latency-bound).
+//  * A third warpgroup copies K and V into TMEM, stages L and D of upcoming
+//    halves into a shared-memory ring, drains each query tile's dQ through a
+//    swizzled staging tile and a TMA reduce-add into the fp32 accumulator,
+//    and writes dK (times scale) and dV at the end.
 //
-// Warps: 0-3 compute (even halves), 4-7 compute (odd halves), 8-11 dQ drain
-// and epilogue, 12 TMA producer, 13 MMA issuer.  448 threads, 1 CTA per SM.
+// Warps: 0-3 compute (query columns 0-31 of each half), 4-7 compute (columns
+// 32-63), 8-11 L/D staging, dQ drain and epilogue, 12 TMA producer, 13 MMA
+// issuer.  448 threads, 1 CTA per SM.
 //
 // Tensor memory (512 columns):
 //   [  0, 64) dK      [ 64,128) dV      [128,160) K bf16   [160,192) V bf16
 //   [192,256) S^T buf0  [256,320) dP^T buf0  [320,384) S^T buf1  [384,448) dP^T buf1
 //   [448,512) dQ of the current query tile
-// P^T (bf16) overwrites the first 32 columns of its S^T buffer, dS^T (bf16)
-// the first 32 columns of its dP^T buffer.
+// Warpgroup w writes its P^T (bf16, 16 columns) at columns [32w, 32w+16) of
+// the S^T buffer, over S^T columns it has itself just read, and its dS^T the
+// same way in the dP^T buffer; the MMAs address the two 16-column pieces.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -45,29 +50,33 @@ struct Cfg64 {
   static constexpr int BK = 128;                 // keys per CTA
   static constexpr int BQ = 128;                 // queries per tile (two halves)
   static constexpr int TILE = 128 * 128;         // 128 rows x 64 bf16
-  static constexpr int NSQ = 2;                  // Q / dO stages
+  static constexpr int NSQ = 3;                  // Q / dO stages
+  // V is only needed until it has been copied into tensor memory; its
+  // region then holds the first box of the dQ staging tile.
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
-  static constexpr int OFF_Q = OFF_V + TILE;
+  static constexpr int OFF_STG = OFF_V;                  // dQ staging: 2 boxes 128 x 32 fp32
+  static constexpr int OFF_Q = OFF_STG + 2 * TILE;
   static constexpr int OFF_DO = OFF_Q + NSQ * TILE;
   static constexpr int OFF_DS = OFF_DO + NSQ * TILE;  // 2 x (128 keys x 128 queries bf16)
   static constexpr int DS_BYTES = 2 * TILE;
-  static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;  // dQ staging: 2 boxes 128 x 32 fp32
-  // per compute warpgroup, two slots (alternate half-steps): L[64], D[64]
-  static constexpr int OFF_LD = OFF_STG + 2 * TILE;
-  static constexpr int OFF_BAR = OFF_LD + 2 * 2 * 128 * 4;
+  // L/D ring: NLD slots of one half-step each, L*log2e[64] then D[64]
+  static constexpr int NLD = 6;
+  static constexpr int OFF_LD = OFF_DS + 2 * DS_BYTES;
+  static constexpr int OFF_BAR = OFF_LD + NLD * 128 * 4;
   // barriers
   static constexpr int B_KV = 0;
-  static constexpr int B_KVT = 1;                 // K, V copied into TMEM (128 arrivals)
+  static constexpr int B_KVT = 1;                 // K, V copied into TMEM (4 warp arrivals)
   static constexpr int B_QDFULL = 2;              // [NSQ]
   static constexpr int B_QDEMPTY = B_QDFULL + NSQ;
   static constexpr int B_SDP = B_QDEMPTY + NSQ;   // [2] S^T/dP^T of a half ready
-  static constexpr int B_PDS = B_SDP + 2;         // [2] P^T/dS^T of a half ready (128 arrivals)
+  static constexpr int B_PDS = B_SDP + 2;         // [2] P^T/dS^T of a half ready (8 warp arrivals)
   static constexpr int B_DSFREE = B_PDS + 2;      // [2] dS^T smem buffer of a tile free
   static constexpr int B_DQFULL = B_DSFREE + 2;   // dQ of a tile in TMEM
-  static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ drained (128 arrivals)
-  static constexpr int B_WG = B_DQFREE + 1;       // [3] warpgroup-internal syncs (128 arrivals)
-  static constexpr int B_DRAIN = B_WG + 3;
+  static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ drained (4 warp arrivals)
+  static constexpr int B_WG = B_DQFREE + 1;       // drain-warpgroup internal sync (4 warp arrivals)
+  static constexpr int B_LDFULL = B_WG + 1;       // [NLD] L/D slot filled (4 warp arrivals)
+  static constexpr int B_DRAIN = B_LDFULL + NLD;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -139,19 +148,20 @@ __global__ void __launch_bounds__(448, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_KV), 1);
-    mbar_init(bar(C::B_KVT), 128);
+    mbar_init(bar(C::B_KVT), 4);  // one arrival per warp of the drain warpgroup
     for (int s = 0; s < C::NSQ; ++s) {
       mbar_init(bar(C::B_QDFULL + s), 1);
       mbar_init(bar(C::B_QDEMPTY + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::B_SDP + s), 1);
-      mbar_init(bar(C::B_PDS + s), 128);
+      mbar_init(bar(C::B_PDS + s), 8);  // both compute warpgroups
       mbar_init(bar(C::B_DSFREE + s), 1);
     }
     mbar_init(bar(C::B_DQFULL), 1);
-    mbar_init(bar(C::B_DQFREE), 128);
-    for (int s = 0; s < 3; ++s) mbar_init(bar(C::B_WG + s), 128);
+    mbar_init(bar(C::B_DQFREE), 4);
+    mbar_init(bar(C::B_WG), 4);
+    for (int s = 0; s < C::NLD; ++s) mbar_init(bar(C::B_LDFULL + s), 4);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -211,9 +221,16 @@ __global__ void __launch_bounds__(448, 1)
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
-      constexpr uint32_t id_sdp = idesc_bf16_f32(128, 64, false, false);  // S^T, dP^T
-      constexpr uint32_t id_kv = idesc_bf16_f32(128, 64, false, true);    // dV, dK
-      constexpr uint32_t id_q = idesc_bf16_f32(128, 64, true, true);      // dQ
+      constexpr uint32_t ID_SDP = idesc_bf16_f32(128, 64, false, false);  // S^T, dP^T
+      constexpr uint32_t ID_KV = idesc_bf16_f32(128, 64, false, true);    // dV, dK
+      constexpr uint32_t ID_Q = idesc_bf16_f32(128, 64, true, true);      // dQ
+      // Descriptors built once; k-steps move them by compile-time offsets.
+      const uint64_t q_kmaj = smem_desc_sw128(sQ, 16, 1024);        // Q as K-major B
+      const uint64_t do_kmaj = smem_desc_sw128(sdO, 16, 1024);
+      const uint64_t q_mn = smem_desc_sw128(sQ, C::TILE, 1024);     // Q as MN-major B
+      const uint64_t do_mn = smem_desc_sw128(sdO, C::TILE, 1024);
+      const uint64_t ds_mn = smem_desc_sw128(sDS, C::TILE, 1024);   // dS (query rows) as A
+      const uint64_t k_mn = smem_desc_sw128(sK, C::TILE, 1024);     // K as MN-major B
       bool ok = mbar_wait(bar(C::B_KVT), 0, abort_flag, p.err, kErrTimeoutMma);
       // S^T and dP^T of half h into buffer h & 1.
       auto issue_sdp = [&](int h) -> bool {
@@ -223,16 +240,16 @@ __global__ void __launch_bounds__(448, 1)
           return false;
         tc_fence_after();
         const uint32_t buf = tmem + C::COL_BUF + 128 * (h & 1);
-        const uint32_t q_half = sQ + st * C::TILE + a * 8192;
-        const uint32_t do_half = sdO + st * C::TILE + a * 8192;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(buf, tmem + C::COL_KT + kk * 8, smem_desc_sw128(q_half + kk * 32, 16, 1024),
-                 id_sdp, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(buf + 64, tmem + C::COL_VT + kk * 8, smem_desc_sw128(do_half + kk * 32, 16, 1024),
-                 id_sdp, kk > 0 ? 1u : 0u);
+        const uint32_t off = st * C::TILE + a * 8192;
+        const uint64_t qd = desc_add(q_kmaj, off), dd = desc_add(do_kmaj, off);
+        mma_ts_k<ID_SDP, 0>(buf, tmem + C::COL_KT, qd);
+        mma_ts_k<ID_SDP, 1>(buf, tmem + C::COL_KT + 8, desc_add(qd, 32));
+        mma_ts_k<ID_SDP, 1>(buf, tmem + C::COL_KT + 16, desc_add(qd, 64));
+        mma_ts_k<ID_SDP, 1>(buf, tmem + C::COL_KT + 24, desc_add(qd, 96));
+        mma_ts_k<ID_SDP, 0>(buf + 64, tmem + C::COL_VT, dd);
+        mma_ts_k<ID_SDP, 1>(buf + 64, tmem + C::COL_VT + 8, desc_add(dd, 32));
+        mma_ts_k<ID_SDP, 1>(buf + 64, tmem + C::COL_VT + 16, desc_add(dd, 64));
+        mma_ts_k<ID_SDP, 1>(buf + 64, tmem + C::COL_VT + 24, desc_add(dd, 96));
         mma_commit(bar(C::B_SDP + (h & 1)));
         return true;
       };
@@ -243,18 +260,28 @@ __global__ void __launch_bounds__(448, 1)
         if (!mbar_wait(bar(C::B_PDS + a), (h >> 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
         tc_fence_after();
         const uint32_t buf = tmem + C::COL_BUF + 128 * a;
-        const uint32_t q_half = sQ + st * C::TILE + a * 8192;
-        const uint32_t do_half = sdO + st * C::TILE + a * 8192;
+        const uint32_t off = st * C::TILE + a * 8192;
+        const uint64_t qd = desc_add(q_mn, off), dd = desc_add(do_mn, off);
         // dV += P^T dO_h ; dK += dS^T Q_h  (64 queries = 4 steps of 16)
+        // P^T / dS^T of queries 16kk.. sit at columns (kk/2)*32 + (kk%2)*8.
+        if (h == 0) {
+          mma_ts_k<ID_KV, 0>(tmem + C::COL_DV, buf, dd);
+          mma_ts_k<ID_KV, 0>(tmem + C::COL_DK, buf + 64, qd);
+        } else {
+          mma_ts_k<ID_KV, 1>(tmem + C::COL_DV, buf, dd);
+          mma_ts_k<ID_KV, 1>(tmem + C::COL_DK, buf + 64, qd);
+        }
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + C::COL_DV, buf + kk * 8, smem_desc_sw128(do_half + kk * 2048, 16384, 1024),
-                 id_kv, (h > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + C::COL_DK, buf + 64 + kk * 8,
-                 smem_desc_sw128(q_half + kk * 2048, 16384, 1024), id_kv,
-                 (h > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 1; kk < 4; ++kk) {
+          const uint32_t col = (kk >> 1) * 32 + (kk & 1) * 8;
+          mma_ts_k<ID_KV, 1>(tmem + C::COL_DV, buf + col, desc_add(dd, kk * 2048));
+          mma_ts_k<ID_KV, 1>(tmem + C::COL_DK, buf + 64 + col, desc_add(qd, kk * 2048));
+        }
+        // Q_h and dO_h of the tile are not read after the second half's dV/dK.
+        if (a == 1) mma_commit(bar(C::B_QDEMPTY + st));
+        // Queue the next S^T/dP^T before possibly waiting for the dQ drain, so
+        // that the tensor core keeps working meanwhile.
+        if (h + 2 < n_half && !issue_sdp(h + 2)) break;
         if (a == 1) {
           if (s > 0) {
             if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma))
@@ -262,16 +289,14 @@ __global__ void __launch_bounds__(448, 1)
             tc_fence_after();
           }
           // dQ = dS K_j: A = dS (query rows) read MN-major from the dS^T tile.
-          const uint32_t ds = sDS + (s & 1) * C::DS_BYTES;
+          const uint64_t dsd = desc_add(ds_mn, (s & 1) * C::DS_BYTES);
+          mma_ss_k<ID_Q, 0>(tmem + C::COL_DQ, dsd, k_mn);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::COL_DQ, smem_desc_sw128(ds + kk * 2048, C::TILE, 1024),
-                   smem_desc_sw128(sK + kk * 2048, C::TILE, 1024), id_q, kk > 0 ? 1u : 0u);
+          for (int kk = 1; kk < 8; ++kk)
+            mma_ss_k<ID_Q, 1>(tmem + C::COL_DQ, desc_add(dsd, kk * 2048), desc_add(k_mn, kk * 2048));
           mma_commit(bar(C::B_DQFULL));
           mma_commit(bar(C::B_DSFREE + (s & 1)));
-          mma_commit(bar(C::B_QDEMPTY + st));
         }
-        if (h + 2 < n_half && !issue_sdp(h + 2)) break;
       }
       if (*abort_flag) {
         mma_commit(bar(C::B_DRAIN));
@@ -280,84 +305,77 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else if (wg < 2) {
     // ------------------------------------------------------------ compute (key rows)
+    // Warpgroup wg handles query columns [32 wg, 32 wg + 32) of every half.
     const int t = threadIdx.x & 127;  // key row
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int key = jt * C::BK + t;
     const bool key_live = key < p.N;
     const float c = p.scale_log2;
-    // L[64], D[64] of the current half; two slots so that a fast thread
-    // filling the next half cannot overwrite values a slow thread still reads
-    float* sLD0 = reinterpret_cast<float*>(smem + C::OFF_LD + wg * 1024);
-    uint32_t wg_phase = 0;
     bool ok = true;
-    // prefetch of this warpgroup's first half: thread t < 64 loads L, t >= 64 loads D
-    auto fetch = [&](int h) -> float {
-      const int s = h >> 1;
+    for (int h = 0; h < n_half; ++h) {
+      const int s = h >> 1, a = h & 1;
       int bhq, it;
       step_coords(s, bhq, it);
-      const int qrow = it * C::BQ + (h & 1) * 64 + (t & 63);
-      if (qrow >= p.N) return t < 64 ? INFINITY : 0.0f;  // dead rows: P = 0
-      const size_t idx = static_cast<size_t>(bhq) * p.N + qrow;
-      return t < 64 ? p.lse[idx] * kLog2e : p.Dvec[idx];
-    };
-    float pre = (wg < n_half) ? fetch(wg) : 0.0f;
-    for (int h = wg; h < n_half; h += 2) {
-      const int s = h >> 1;
-      int bhq, it;
-      step_coords(s, bhq, it);
-      const int q0 = it * C::BQ + (h & 1) * 64;
-      float* sLD = sLD0 + ((h >> 1) & 1) * 128;
-      sLD[t] = pre;
-      if (h + 2 < n_half) pre = fetch(h + 2);
-      mbar_arrive(bar(C::B_WG + wg));
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_WG + wg), wg_phase & 1, abort_flag, p.err,
+      const int q0 = it * C::BQ + a * 64 + wg * 32;  // first query of this warpgroup's columns
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SDP + a), (h >> 1) & 1, abort_flag, p.err,
                                              kErrTimeoutSoftmax));
-      ++wg_phase;
       if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SDP + wg), (h >> 1) & 1, abort_flag,
-                                             p.err, kErrTimeoutSoftmax));
-      if (!ok) break;
-      if (s >= 2) {  // the dS^T buffer of tile s - 2 must have been read by its dQ MMA
+      if (s >= 2 && a == 0) {  // the dS^T buffer of tile s - 2 must have been read by its dQ MMA
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DSFREE + (s & 1)), ((s - 2) >> 1) & 1,
                                                abort_flag, p.err, kErrTimeoutSoftmax));
         if (!ok) break;
       }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_LDFULL + h % C::NLD), (h / C::NLD) & 1,
+                                             abort_flag, p.err, kErrTimeoutSoftmax));
+      if (!ok) break;
       tc_fence_after();
-      const uint32_t buf = tmem + lane_off + C::COL_BUF + 128 * wg;
-      const bool diag = CAUSAL && (it == jt);
-      const uint32_t ds_blk = sDS + (s & 1) * C::DS_BYTES + wg * C::TILE;
+      const uint32_t sbuf = tmem + lane_off + C::COL_BUF + 128 * a + 32 * wg;
+      const float* slot = reinterpret_cast<const float*>(smem + C::OFF_LD) + (h % C::NLD) * 128;
+      const float4* L4 = reinterpret_cast<const float4*>(slot + 32 * wg);
+      const float4* D4 = reinterpret_cast<const float4*>(slot + 64 + 32 * wg);
+      uint32_t sv[32], dpv[32];
+      tmem_ld32(sbuf, sv);
+      tmem_ld32(sbuf + 64, dpv);
+      // Masking is needed only on the diagonal tile and for keys past N;
+      // warp-uniform, so the common case runs without per-element tests.
+      const bool masked = __any_sync(0xffffffffu, (CAUSAL && it == jt) || !key_live);
+      tmem_wait_ld();
+      uint32_t pk[16], dk16[16];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(buf + cc * 32, sv);
-        tmem_ld32(buf + 64 + cc * 32, dpv);
-        tmem_wait_ld();
-        uint32_t pk[16], dk16[16];
+      for (int u4 = 0; u4 < 8; ++u4) {
+        const float4 l4 = L4[u4];
+        const float4 d4 = D4[u4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pv[4], dsv[4];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          float pv[2], dsv[2];
+        for (int e = 0; e < 4; ++e)
+          pv[e] = ex2_approx(fmaf(__uint_as_float(sv[u4 * 4 + e]), c, -lv[e]));
+        if (masked) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int qq = cc * 32 + 2 * u + e;
-            float pr = ex2_approx(fmaf(__uint_as_float(sv[2 * u + e]), c, -sLD[qq]));
-            if (!key_live || (diag && key > q0 + qq)) pr = 0.0f;
-            pv[e] = pr;
-            dsv[e] = pr * (__uint_as_float(dpv[2 * u + e]) - sLD[64 + qq]);
-          }
-          pk[u] = pack_bf16x2(pv[0], pv[1]);
-          dk16[u] = pack_bf16x2(dsv[0], dsv[1]);
+          for (int e = 0; e < 4; ++e)
+            if (!key_live || (CAUSAL && key > q0 + u4 * 4 + e)) pv[e] = 0.0f;
         }
-        tmem_st16(buf + cc * 16, pk);          // P^T over S^T
-        tmem_st16(buf + 64 + cc * 16, dk16);   // dS^T over dP^T
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          st_shared_v4(ds_blk + sw128(t, cc * 4 + q4), dk16[4 * q4], dk16[4 * q4 + 1],
-                       dk16[4 * q4 + 2], dk16[4 * q4 + 3]);
+        for (int e = 0; e < 4; ++e)
+          dsv[e] = pv[e] * (__uint_as_float(dpv[u4 * 4 + e]) - dv4[e]);
+        pk[2 * u4] = pack_bf16x2(pv[0], pv[1]);
+        pk[2 * u4 + 1] = pack_bf16x2(pv[2], pv[3]);
+        dk16[2 * u4] = pack_bf16x2(dsv[0], dsv[1]);
+        dk16[2 * u4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
       }
+      tmem_st16(sbuf, pk);         // P^T over this warpgroup's S^T columns
+      tmem_st16(sbuf + 64, dk16);  // dS^T over its dP^T columns
+      // dS^T row t, queries 32wg .. 32wg+31 of the half: chunks 4wg..4wg+3 of block a.
+      const uint32_t ds_blk = sDS + (s & 1) * C::DS_BYTES + a * C::TILE;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        st_shared_v4(ds_blk + sw128(t, wg * 4 + q4), dk16[4 * q4], dk16[4 * q4 + 1],
+                     dk16[4 * q4 + 2], dk16[4 * q4 + 3]);
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(C::B_PDS + wg));
+      mbar_arrive_warp(bar(C::B_PDS + a));
     }
   } else if (wg == 2) {
     // ------------------------------------------------------------ K/V -> TMEM, dQ drain, epilogue
@@ -384,17 +402,40 @@ __global__ void __launch_bounds__(448, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(C::B_KVT));
+      mbar_arrive_warp(bar(C::B_KVT));
     }
     auto wg_sync = [&]() -> bool {
-      mbar_arrive(bar(C::B_WG + 2));
-      const bool r = mbar_wait(bar(C::B_WG + 2), wg_phase & 1, abort_flag, p.err, kErrTimeoutOther);
+      mbar_arrive_warp(bar(C::B_WG));
+      const bool r = mbar_wait(bar(C::B_WG), wg_phase & 1, abort_flag, p.err, kErrTimeoutOther);
       ++wg_phase;
       return __all_sync(0xffffffffu, r);
     };
+    // L*log2e and D of half h into ring slot h % NLD: thread t < 64 loads L
+    // of query t of the half, t >= 64 loads D of query t - 64.  Rows past N
+    // get L = +inf (so P = 0) and D = 0.
+    auto load_ld = [&](int h) -> float {
+      if (h >= n_half) return 0.0f;
+      int bhq, it;
+      step_coords(h >> 1, bhq, it);
+      const int qrow = it * C::BQ + (h & 1) * 64 + (t & 63);
+      if (qrow >= p.N) return t < 64 ? INFINITY : 0.0f;
+      const size_t idx = static_cast<size_t>(bhq) * p.N + qrow;
+      return t < 64 ? p.lse[idx] * kLog2e : p.Dvec[idx];
+    };
+    auto store_ld = [&](int h, float val) {
+      if (h >= n_half) return;
+      reinterpret_cast<float*>(smem + C::OFF_LD)[(h % C::NLD) * 128 + t] = val;
+      mbar_arrive_warp(bar(C::B_LDFULL + h % C::NLD));
+    };
+    // Halves of tiles 0..2 first; after draining tile s, the halves of tile
+    // s + 3 (their slots held tile s, whose halves are done by then).  The
+    // loads for tile s + 3 are issued before waiting for tile s.
+    for (int h = 0; h < C::NLD; ++h) store_ld(h, load_ld(h));
     for (int s = 0; ok && s < n_steps; ++s) {
       int bhq, it;
       step_coords(s, bhq, it);
+      const float ld_next0 = load_ld(2 * (s + 3));
+      const float ld_next1 = load_ld(2 * (s + 3) + 1);
       ok = __all_sync(0xffffffffu,
                       mbar_wait(bar(C::B_DQFULL), s & 1, abort_flag, p.err, kErrTimeoutOther));
       if (!ok) break;
@@ -404,7 +445,7 @@ __global__ void __launch_bounds__(448, 1)
       tmem_ld32(tmem + lane_off + C::COL_DQ + 32, bb);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar(C::B_DQFREE));  // dQ columns may be overwritten now
+      mbar_arrive_warp(bar(C::B_DQFREE));  // dQ columns may be overwritten now
       if (t == 0) bulk_wait_group_read0();  // staging free again
       if (!(ok = wg_sync())) break;
 #pragma unroll
@@ -420,8 +461,13 @@ __global__ void __launch_bounds__(448, 1)
         tma_reduce_add_3d(&tmdQ, sSTG + C::TILE, 32, it * C::BQ, bhq);
         bulk_commit_group();
       }
+      // dQ of tile s in TMEM means both halves of tile s were consumed, so the
+      // ring slots of tile s can take tile s + 3.
+      store_ld(2 * (s + 3), ld_next0);
+      store_ld(2 * (s + 3) + 1, ld_next1);
     }
     if (t == 0) bulk_wait_group0();
+    __syncwarp();  // lane 0 waited alone; the TMEM loads below are warp-collective
     // ---- epilogue: every MMA has completed once the last dQ was seen
     if (ok) {
       tc_fence_after();
@@ -455,6 +501,9 @@ __global__ void __launch_bounds__(448, 1)
     }
   }
 
+  // Every warp reconverges first: in the TMA and MMA warps only one lane did
+  // the work, and the CTA barrier below must count whole, converged warps.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 13) {

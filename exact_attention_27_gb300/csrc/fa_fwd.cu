@@ -60,7 +60,7 @@ struct FwdCfg {
   static constexpr int SUB = D / 64;             // 128-byte column blocks per row
   static constexpr int SUB_BYTES = 128 * 128;    // one 128-row x 64-col bf16 block
   static constexpr int TILE = SUB * SUB_BYTES;   // one 128 x D bf16 tile
-  static constexpr int NS = (D == 64) ? 4 : 2;   // K/V ring stages
+  static constexpr int NS = (D == 64) ? 4 : 3;   // K/V ring stages
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
@@ -91,6 +91,8 @@ struct FwdParams {
   int G;          // query heads per key/value head
   int n_qtiles;
   int n_ktiles;
+  int n_heads;          // B * Hq
+  int heads_per_group;  // launch-order grouping, a multiple of G
   float scale_log2;  // scale * log2(e)
   uint32_t* err;
 };
@@ -109,11 +111,15 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5;
-  // Launch order: head-major, so the CTAs in flight at any time share the
-  // K/V of a few heads (which then stay in L2); within a head the heaviest
-  // causal tiles come first.
-  const int bh = static_cast<int>(blockIdx.x) / p.n_qtiles;  // flattened (batch, query head)
-  const int qi_ = static_cast<int>(blockIdx.x) - bh * p.n_qtiles;
+  // Launch order: heads are taken in groups of p.heads_per_group (sized on
+  // the host so that the group's K/V fits comfortably in L2); within a group
+  // the heaviest causal query tiles of all its heads come first.
+  const int per_group = p.heads_per_group * p.n_qtiles;
+  const int grp = static_cast<int>(blockIdx.x) / per_group;
+  const int rem = static_cast<int>(blockIdx.x) - grp * per_group;
+  const int in_grp = min(p.heads_per_group, p.n_heads - grp * p.heads_per_group);
+  const int qi_ = rem / in_grp;
+  const int bh = grp * p.heads_per_group + (rem - qi_ * in_grp);  // flattened (batch, query head)
   const int qt = CAUSAL ? (p.n_qtiles - 1 - qi_) : qi_;
   const int b = bh / p.Hq;
   const int hq = bh - b * p.Hq;
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::B_SFULL + s), 1);
-      mbar_init(bar(C::B_PFULL + s), 128);
+      mbar_init(bar(C::B_PFULL + s), 4);  // one arrival per softmax warp
     }
     mbar_init(bar(C::B_ODONE), 1);
     mbar_init(bar(C::B_DRAIN), 1);
@@ -195,8 +201,12 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t ID_O = idesc_bf16_f32(128, D, false, true);
+      // Descriptors built once; k-steps move them by compile-time offsets.
+      const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t k_desc = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t v_desc = smem_desc_sw128(sV, C::SUB_BYTES, 1024);
       bool ok = mbar_wait(bar(C::B_QFULL), 0, abort_flag, p.err, kErrTimeoutMma);
       // S_j = Q K_j^T into S buffer j & 1; frees the K stage when done.
       auto issue_s = [&](int j) -> bool {
@@ -205,11 +215,12 @@ __global__ void __launch_bounds__(192, 1)
           return false;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (j & 1) * 128;
+        const uint64_t kd = desc_add(k_desc, st * C::TILE);
+        mma_ss_k<ID_S, 0>(d_tmem, q_desc, kd);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 1; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          mma_ss(d_tmem, smem_desc_sw128(sQ + off, 16, 1024),
-                 smem_desc_sw128(sK + st * C::TILE + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss_k<ID_S, 1>(d_tmem, desc_add(q_desc, off), desc_add(kd, off));
         }
         mma_commit(bar(C::B_SFULL + (j & 1)));
         mma_commit(bar(C::B_KEMPTY + st));
@@ -225,14 +236,17 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
           break;
         tc_fence_after();
+        // P occupies 64 packed columns; 16 keys = 8 columns per step.
+        // V block: 16 key rows of 128 bytes per step; D/64 blocks 16 KB apart.
+        const uint64_t vd = desc_add(v_desc, st * C::TILE);
+        const uint32_t pa = tmem + sb * 128;
+        if (j == 0)
+          mma_ts_k<ID_O, 0>(tmem + C::COL_O, pa, vd);
+        else
+          mma_ts_k<ID_O, 1>(tmem + C::COL_O, pa, vd);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // P occupies 64 packed columns; 16 keys = 8 columns per step.
-          // V block: 16 key rows of 128 bytes per step; D/64 blocks 16 KB apart.
-          mma_ts(tmem + C::COL_O, tmem + sb * 128 + kk * 8,
-                 smem_desc_sw128(sV + st * C::TILE + kk * 2048, C::SUB_BYTES, 1024), idesc_o,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < 8; ++kk)
+          mma_ts_k<ID_O, 1>(tmem + C::COL_O, pa + kk * 8, desc_add(vd, kk * 2048));
         mma_commit(bar(C::B_ODONE));
         mma_commit(bar(C::B_VEMPTY + st));
       }
@@ -324,7 +338,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(C::B_PFULL + sb));
+      mbar_arrive_warp(bar(C::B_PFULL + sb));
     }
     // ------------------------------------------------------------ epilogue
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE), (n_kv - 1) & 1, abort_flag,
@@ -355,6 +369,9 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
+  // Every warp reconverges first: in the TMA and MMA warps only one lane did
+  // the work, and the CTA barrier below must count whole, converged warps.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {
@@ -383,6 +400,18 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   p.n_ktiles = (s.N + C::BN - 1) / C::BN;
   p.scale_log2 = s.scale * kLog2e;
   p.err = err;
+  p.n_heads = s.B * s.Hq;
+  {
+    // Group query heads so that the K/V they read (shared within a GQA
+    // group) stays within about 48 MiB of the 129 MB L2.
+    const double kv_bytes = 2.0 * s.N * D * 2.0;  // one K/V head
+    const double budget = 48.0 * 1024 * 1024;
+    long long kv_heads = static_cast<long long>(budget / kv_bytes);
+    if (kv_heads < 1) kv_heads = 1;
+    long long hpg = kv_heads * p.G;
+    if (hpg > p.n_heads) hpg = p.n_heads;
+    p.heads_per_group = static_cast<int>(hpg);
+  }
   const long long grid = static_cast<long long>(s.B) * s.Hq * p.n_qtiles;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);

@@ -62,6 +62,14 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One arrival per warp: the warp's lanes synchronise, then lane 0 arrives.
+// Each lane's earlier shared-memory writes and tcgen05 operations (after its
+// own fence) are ordered before the arrival by the warp synchronisation.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  __syncwarp();
+  if (lane_id() == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                "r"(bytes)
@@ -80,6 +88,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, but a thread whose phase is not complete is suspended (until
+// the phase completes, or for at most about kSuspendHintNs) instead of
+// returning at once, so that waiting warps do not take issue slots from the
+// warps doing work.
+constexpr uint32_t kSuspendHintNs = 1000000;  // 1 ms
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of parity `parity` to complete.  Gives up when the
 // shared abort word is set by another role or after kWaitLimitNs; then sets
 // the abort word, ORs `code` into the device error word and returns false.
@@ -88,9 +114,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
@@ -104,7 +128,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // let copies and MMAs already in flight land before the CTA exits).
 __device__ __forceinline__ bool mbar_wait_timed(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
+  while (!mbar_try_wait_sleep(bar, parity))
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   return true;
 }
@@ -263,6 +287,34 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Same with the instruction descriptor and the accumulate flag as
+// compile-time constants (fewer instructions on the issuing thread).
+template <uint32_t IDESC, uint32_t ACC>
+__device__ __forceinline__ void mma_ss_k(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "n"(IDESC), "n"(ACC)
+      : "memory");
+}
+
+template <uint32_t IDESC, uint32_t ACC>
+__device__ __forceinline__ void mma_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "n"(IDESC), "n"(ACC)
+      : "memory");
+}
+
+// A shared-memory descriptor moved by `bytes` (a multiple of 16): only the
+// start-address field changes, and it cannot overflow for addresses < 256 KB.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
 }
 
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread completes.
