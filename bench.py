@@ -34,7 +34,7 @@ STEP_WORKLOAD = "causal_train_n4096_d64"
 FWD_WORKLOADS = ["causal_n4096_d64", "causal_n8192_d128", "causal_gqa_n16384_d128"]
 FALLBACK_TFLOPS = 1900.0
 FALLBACK_GBS = 6800.0
-L2_FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 * 10**6
 
 
 # ------------------------------------------------------------------ helpers
@@ -127,6 +127,12 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 
+def _rotation(bytes_per_set):
+    """Number of input sets to cycle through so that a step's inputs were
+    evicted from the 129 MB L2 by the steps before it (at least 3x L2)."""
+    return max(1, math.ceil(3 * L2_BYTES / bytes_per_set))
+
+
 def run_ours(args, rank, world):
     import torch
     import exact_attention_27_gb300 as fa
@@ -141,44 +147,54 @@ def run_ours(args, rank, world):
     w = WORKLOADS[STEP_WORKLOAD]
     stream = torch.cuda.current_stream()
     inp = make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, seed=rank * 100, with_grad=True)
-    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    base = {n: inp[n].cuda() for n in ("q", "k", "v", "do")}
+
+    def new_set():
+        t = {n: x.clone() for n, x in base.items()}
+        t["o"] = torch.empty_like(t["q"])
+        t["lse"] = torch.empty(t["q"].shape[:-1], dtype=torch.float32, device="cuda")
+        t["dq"], t["dk"], t["dv"] = (torch.empty_like(t["q"]), torch.empty_like(t["k"]),
+                                     torch.empty_like(t["v"]))
+        return t
+
+    first = new_set()
+    set_bytes = sum(x.numel() * x.element_size() for x in first.values())
+    R = _rotation(set_bytes)
+    sets = [first] + [new_set() for _ in range(R - 1)]
     flops_fwd, flops_bwd = w.fwd_flops(), w.bwd_flops()
 
-    def step():
-        fa.fa_forward(q, k, v, o, lse, w.scale, True)
-        fa.fa_backward(q, k, v, o, lse, do, dq, dk, dv, w.scale, True)
+    def step(t, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_forward(t["q"], t["k"], t["v"], t["o"], t["lse"], w.scale, True)
+        if ev is not None:
+            ev[1].record(stream)
+            fa.fa_set_backward_events(ev[2], ev[3])
+        fa.fa_backward(t["q"], t["k"], t["v"], t["o"], t["lse"], t["do"], t["dq"], t["dk"],
+                       t["dv"], w.scale, True)
 
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        step()
+    for i in range(args.warmup):
+        step(sets[i % R])
     torch.cuda.synchronize()
     if fa.fa_last_device_error() != 0:
         raise RuntimeError("device error during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     for e in ev:  # create the events (torch creates them on first record)
         for x in e:
             x.record(stream)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev) as clocks:
         t_wall = time.perf_counter()
+        t_start.record(stream)
         for i in range(K):
-            flush.fill_(float(i))  # L2 flush, outside the step's events
-            e = ev[i]
-            e[0].record(stream)
-            fa.fa_forward(q, k, v, o, lse, w.scale, True)
-            e[1].record(stream)
-            fa.fa_set_backward_events(e[2], e[3])
-            fa.fa_backward(q, k, v, o, lse, do, dq, dk, dv, w.scale, True)
-            e[4].record(stream)
+            step(sets[(args.warmup + i) % R], ev[i])
+        t_end.record(stream)
         fa.fa_set_backward_events(None, None)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
@@ -186,11 +202,9 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     if fa.fa_last_device_error() != 0:
         raise RuntimeError("device error during the timed steps")
-    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    total_ms = t_start.elapsed_time(t_end)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    bwd_ms = [e[1].elapsed_time(e[4]) for e in ev]
     bwd_main_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -202,14 +216,13 @@ def run_ours(args, rank, world):
     fwd_avg = statistics.mean(fwd_ms)
     bwd_main_avg = statistics.mean(bwd_main_ms)
     if bwd_main_avg >= fwd_avg:
-        kname, kflops, kms = "fa_bwd_kernel<64,causal>", flops_bwd, bwd_main_avg
+        kname, kflops, kms = "fa_bwd64_kernel<causal>", flops_bwd, bwd_main_avg
     else:
         kname, kflops, kms = "fa_fwd_kernel<64,causal>", flops_fwd, fwd_avg
     achieved = kflops / (kms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": tflops_peak, "unit": "TFLOP/s", "frac": round(achieved / tflops_peak, 4),
-                "peak_source": f"{peak_src} bf16 burst",
-                "traffic": kernel_traffic(kname.split("<")[0] + "<64,causal>")}
+                "peak_source": f"{peak_src} bf16 burst", "traffic": kernel_traffic(kname)}
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -219,14 +232,18 @@ def run_ours(args, rank, world):
         "config": {"workload": w.describe(), "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "N": w.N,
                    "d": w.d, "causal": True, "step": "fa_forward + fa_backward",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed before every step (512 MiB write), flush outside the timing",
+                   "l2": f"inputs larger than L2: {R} rotating input sets of "
+                         f"{set_bytes / 2**20:.0f} MiB, steps back to back",
                    "frac_of_peak": round(value / world / tflops_peak, 4)},
-        "fwd_ms": round(fwd_avg, 5), "bwd_ms": round(statistics.mean(bwd_ms), 5),
+        "fwd_ms": round(fwd_avg, 5),
+        "bwd_ms": round(ms_per_step - fwd_avg, 5),
         "bwd_main_kernel_ms": round(bwd_main_avg, 5),
         "roofline": roofline,
         "gpu_launches": 4 * K,
         "wall_s_timed_region": round(t_wall, 4),
     }
+    del sets, first, base
+    torch.cuda.empty_cache()
     if rank == 0:
         result["clocks"] = clocks.summary()
         if not args.only_step:
@@ -264,34 +281,39 @@ def run_forward_only(args):
 
 
 def forward_workloads(fa, torch, tflops_peak, peak_src):
-    """Forward-only throughput on the larger workloads (inputs larger than L2
-    for the d = 128 ones; L2 flushed before each launch for the smallest)."""
+    """Forward-only throughput on the larger workloads: back-to-back launches,
+    cycling through enough input sets that each launch's inputs come from HBM."""
     out = []
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     for name in FWD_WORKLOADS:
         w = WORKLOADS[name]
         inp = make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, seed=7)
-        q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-        o = torch.empty_like(q)
-        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
-        for _ in range(3):
-            fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
-        reps = 20
-        times = []
-        for _ in range(reps):
-            flush.fill_(0.0)
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s.record()
-            fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
-            e.record()
-            times.append((s, e))
+        per_set = sum(t.numel() * t.element_size() for t in inp.values()) * 4 // 3
+        R = _rotation(per_set)
+        sets = []
+        for _ in range(R):
+            t = {n: x.cuda() for n, x in inp.items()}
+            t["o"] = torch.empty_like(t["q"])
+            t["lse"] = torch.empty(t["q"].shape[:-1], dtype=torch.float32, device="cuda")
+            sets.append(t)
+        for i in range(3):
+            t = sets[i % R]
+            fa.fa_forward(t["q"], t["k"], t["v"], t["o"], t["lse"], w.scale, w.causal)
+        reps = 30
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
-        ms = statistics.mean(s.elapsed_time(e) for s, e in times)
+        s_ev.record()
+        for i in range(reps):
+            t = sets[i % R]
+            fa.fa_forward(t["q"], t["k"], t["v"], t["o"], t["lse"], w.scale, w.causal)
+        e_ev.record()
+        torch.cuda.synchronize()
+        ms = s_ev.elapsed_time(e_ev) / reps
         tf = w.fwd_flops() / (ms * 1e-3) / 1e12
         out.append({"workload": w.describe(), "ms": round(ms, 4), "tflops": round(tf, 1),
-                    "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst"})
-        del q, k, v, o, lse, inp
-    torch.cuda.empty_cache()
+                    "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst",
+                    "input_sets": R})
+        del sets, inp
+        torch.cuda.empty_cache()
     return out
 
 
@@ -375,7 +397,7 @@ def cpu_baseline(w):
     workload: forward + backward of 256-row query blocks in all 16 heads."""
     import oracle
     q_block, flops, secs, steps = 256, 0.0, 0.0, 0
-    while secs < 10.0 and steps < 16:
+    while secs < 10.0 and steps < 64:
         f, dt = oracle_sample(w, q_block, steps)
         flops += f
         secs += dt
