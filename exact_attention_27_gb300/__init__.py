@@ -18,7 +18,7 @@ import math
 from ._lib import FaError, library, status_string  # noqa: F401
 
 __all__ = [
-    "FaError", "fa_forward", "fa_backward", "fa_backward_preprocess", "fa_status_string",
+    "FaError", "fa_forward", "fa_forward_ex", "fa_backward", "fa_backward_preprocess", "fa_status_string",
     "fa_last_device_error", "fa_selftest_wait_timeout", "fa_set_backward_events", "attention_forward", "attention_backward",
     "library",
 ]
@@ -82,6 +82,25 @@ def fa_forward(q, k, v, o, lse, scale, causal, stream=None):
                                 int(bool(causal)), _stream(stream)), "fa_forward")
 
 
+def fa_forward_ex(q, k, v, o, lse, scale, causal, q_offset=0, stream=None):
+    """fa_forward_ex of include/fa.h: q [B,H_q,N_q,d] against k/v [B,H_kv,N_kv,d]."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be [B, H, N, d]")
+    B, Hq, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k must be [B, H_kv, N_kv, d] with q's B and d")
+    Hkv, Nk = k.shape[1], k.shape[2]
+    _bf16_cuda("q", q)
+    _bf16_cuda("k", k)
+    _bf16_cuda("v", v, k.shape)
+    _bf16_cuda("o", o, q.shape)
+    _f32_cuda("lse", lse, (B, Hq, Nq))
+    _check(library().fa_forward_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, Hq, Hkv, Nq, Nk, d, ctypes.c_float(scale),
+                                   int(bool(causal)), int(q_offset), _stream(stream)),
+           "fa_forward_ex")
+
+
 def fa_backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, stream=None):
     """fa_backward of include/fa.h on torch tensors; writes dq, dk, dv."""
     B, Hq, Hkv, N, d = _shapes(q, k)
@@ -128,14 +147,18 @@ def fa_set_backward_events(before, after):
     library().fa_set_backward_events(h(before), h(after))
 
 
-def attention_forward(q, k, v, causal=False, scale=None, stream=None):
-    """Allocates o and lse on q's device and runs fa_forward; returns (o, lse)."""
+def attention_forward(q, k, v, causal=False, scale=None, q_offset=None, stream=None):
+    """Allocates o and lse on q's device and runs fa_forward (or fa_forward_ex
+    when q and k differ in length or a query offset is given); returns (o, lse)."""
     import torch
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
-    fa_forward(q, k, v, o, lse, scale, causal, stream)
+    if q_offset is None and q.shape[2] == k.shape[2]:
+        fa_forward(q, k, v, o, lse, scale, causal, stream)
+    else:
+        fa_forward_ex(q, k, v, o, lse, scale, causal, q_offset or 0, stream)
     return o, lse
 
 

@@ -37,6 +37,8 @@ def _declare(lib):
     p, i, f, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
     lib.fa_forward.restype = i
     lib.fa_forward.argtypes = [p, p, p, p, p, i, i, i, i, i, f, i, p]
+    lib.fa_forward_ex.restype = i
+    lib.fa_forward_ex.argtypes = [p, p, p, p, p, i, i, i, i, i, i, f, i, i, p]
     lib.fa_backward.restype = i
     lib.fa_backward.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, p]
     lib.fa_backward_noalloc.restype = i

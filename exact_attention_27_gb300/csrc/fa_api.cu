@@ -147,6 +147,32 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
                                                                                : FA_ERR_CUDA;
 }
 
+fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H_q, int H_kv, int N_q, int N_kv, int d, float scale, int causal,
+                        int q_offset, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARGUMENT;
+  fa_status st = validate(B, H_q, H_kv, N_q, d, scale, causal);
+  if (st != FA_OK) return st;
+  if (N_kv < 1 || q_offset < 0) return FA_ERR_INVALID_ARGUMENT;
+  if (static_cast<double>(q_offset) + N_q + 128 >= 2147483647.0) return FA_ERR_INVALID_ARGUMENT;
+  if (static_cast<double>(B) * H_kv * N_kv * d >= 1099511627776.0) return FA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_INVALID_ARGUMENT;
+  CUtensorMap tq, tk, tv;
+  if (!make_map_bf16(&tq, q, d, N_q, static_cast<long long>(B) * H_q) ||
+      !make_map_bf16(&tk, k, d, N_kv, static_cast<long long>(B) * H_kv) ||
+      !make_map_bf16(&tv, v, d, N_kv, static_cast<long long>(B) * H_kv))
+    return FA_ERR_CUDA;
+  uint32_t* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  fa::AttnShape s{B, H_q, H_kv, N_q, d, scale, causal};
+  s.Nk = N_kv;
+  s.q_offset = q_offset;
+  return fa::launch_forward(tq, tk, tv, o, lse, s, err, stream) == cudaSuccess ? FA_OK
+                                                                               : FA_ERR_CUDA;
+}
+
 fa_status fa_backward_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
                                  cudaStream_t stream) {
   if (!o || !dO || !D || rows < 1) return FA_ERR_INVALID_ARGUMENT;

@@ -33,8 +33,11 @@
 //
 // Causal masking ("L'attention fusionnee", same section: tiles that lie wholly
 // in the future are never visited; the mask is positional, no mask tensor):
-// query tile i visits key tiles 0..i only; the diagonal tile masks key > query.
-// Keys at or past N (ragged tail) are masked too.
+// query row i sits at absolute position q_offset + i (the input_pos of the
+// CUDA Tile kernel; 0 when queries and keys are the same sequence) and sees
+// keys j <= q_offset + i, so a query tile visits key tiles up to the one
+// holding its last row's position, and only tiles crossing the diagonal are
+// masked.  Keys at or past Nk (ragged tail) are masked too.
 //
 // Every mbarrier wait is bounded (about a second); on expiry the kernel sets
 // an error bit, every role skips its remaining work and the CTA exits.
@@ -86,7 +89,9 @@ struct FwdCfg {
 struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
-  int N;
+  int N;         // query rows
+  int Nk;        // key/value rows
+  int q_offset;  // absolute position of query row 0
   int Hq;
   int G;          // query heads per key/value head
   int n_qtiles;
@@ -124,7 +129,8 @@ __global__ void __launch_bounds__(192, 1)
   const int b = bh / p.Hq;
   const int hq = bh - b * p.Hq;
   const int kvz = b * (p.Hq / p.G) + hq / p.G;  // flattened (batch, kv head)
-  const int n_kv = CAUSAL ? min(qt + 1, p.n_ktiles) : p.n_ktiles;
+  const int n_kv =
+      CAUSAL ? min((p.q_offset + qt * C::BM + C::BM - 1) / C::BN + 1, p.n_ktiles) : p.n_ktiles;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_QFULL), 1);
@@ -285,12 +291,14 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       const int kbase = j * C::BN;
-      const bool need_mask = CAUSAL ? (j == qt || kbase + C::BN > p.N) : (kbase + C::BN > p.N);
+      const int qpos = p.q_offset + qi;  // absolute position of this row
+      const bool need_mask =
+          (kbase + C::BN > p.Nk) || (CAUSAL && kbase + C::BN - 1 > p.q_offset + qt * C::BM);
       if (need_mask) {
 #pragma unroll
         for (int t = 0; t < 128; ++t) {
           const int key = kbase + t;
-          if (key >= p.N || (CAUSAL && key > qi)) s[t] = -INFINITY;
+          if (key >= p.Nk || (CAUSAL && key > qpos)) s[t] = -INFINITY;
         }
       }
       float mx = s[0];
@@ -394,17 +402,19 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.N = s.N;
+  p.Nk = s.keys();
+  p.q_offset = s.q_offset;
   p.Hq = s.Hq;
   p.G = s.Hq / s.Hkv;
   p.n_qtiles = (s.N + C::BM - 1) / C::BM;
-  p.n_ktiles = (s.N + C::BN - 1) / C::BN;
+  p.n_ktiles = (p.Nk + C::BN - 1) / C::BN;
   p.scale_log2 = s.scale * kLog2e;
   p.err = err;
   p.n_heads = s.B * s.Hq;
   {
     // Group query heads so that the K/V they read (shared within a GQA
     // group) stays within about 48 MiB of the 129 MB L2.
-    const double kv_bytes = 2.0 * s.N * D * 2.0;  // one K/V head
+    const double kv_bytes = 2.0 * p.Nk * D * 2.0;  // one K/V head
     const double budget = 48.0 * 1024 * 1024;
     long long kv_heads = static_cast<long long>(budget / kv_bytes);
     if (kv_heads < 1) kv_heads = 1;

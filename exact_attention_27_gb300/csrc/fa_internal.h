@@ -10,9 +10,12 @@
 namespace fa {
 
 struct AttnShape {
-  int B, Hq, Hkv, N, d;
+  int B, Hq, Hkv, N, d;  // N: query rows (and key rows unless Nk says otherwise)
   float scale;
   int causal;
+  int Nk = 0;        // key/value rows; 0 means N
+  int q_offset = 0;  // absolute position of query row 0 under the causal mask
+  int keys() const { return Nk > 0 ? Nk : N; }
 };
 
 // Forward: q/k/v tensor maps (3-D: d, N, B*H; box 64 x 128 x 1; 128-byte

@@ -76,6 +76,25 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
                      cudaStream_t stream);
 
 /*
+ * Forward pass for queries that continue a longer key sequence (prefill
+ * against keys already cached), following the position offset `input_pos` of
+ * the CUDA Tile kernel signature ("Flash Attention ... NVIDIA CUDA Tile",
+ * section "Definiendo la interfaz del kernel").  Query row i sits at absolute
+ * position q_offset + i; with causal = 1 it sees keys j <= q_offset + i, with
+ * causal = 0 every key.  fa_forward(..., N, ...) is fa_forward_ex with
+ * N_q = N_kv = N and q_offset = 0.
+ *
+ *   q, o  [B][H_q][N_q][d]    bf16;   lse [B][H_q][N_q] fp32
+ *   k, v  [B][H_kv][N_kv][d]  bf16
+ *   q_offset >= 0 (every query row then sees at least key 0); N_q, N_kv >= 1.
+ *
+ * Same conventions and return codes as fa_forward.
+ */
+fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H_q, int H_kv, int N_q, int N_kv, int d, float scale, int causal,
+                        int q_offset, cudaStream_t stream);
+
+/*
  * Backward pass.  Source: "L'attention fusionnee", section "La passe
  * arriere : recalculer plutot que garder": P is rebuilt tile by tile from the saved L as p = exp(s - L);
  *   dV = P^T dO;  dS = P o (dO V^T - D) with D = rowsum(dO o O);

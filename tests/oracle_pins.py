@@ -345,10 +345,25 @@ def pin_sampled_rows_match_full(orc):
         assert np.array_equal(l[:, :, rows], l2)
 
 
+def pin_query_offset_is_a_row_block(orc):
+    """Queries at absolute positions o..o+n-1 (N_q = n, offset o, all N_k keys)
+    get exactly rows o..o+n-1 of the full causal result, and a single query at
+    the last position sees every key (the non-causal result for that row)."""
+    q, k, v = _random_problem(800, B=2, Hq=4, Hkv=2, N=29, d=5)
+    o_full, l_full = orc.forward(q, k, v, 0.6, True)
+    for off, n in ((0, 7), (5, 11), (20, 9), (28, 1)):
+        o, l = orc.forward(q[:, :, off:off + n], k, v, 0.6, True, q_offset=off)
+        assert np.array_equal(o, o_full[:, :, off:off + n])
+        assert np.array_equal(l, l_full[:, :, off:off + n])
+    o_nc, l_nc = orc.forward(q[:, :, -1:], k, v, 0.6, False)
+    o_last, l_last = orc.forward(q[:, :, -1:], k, v, 0.6, True, q_offset=28)
+    assert np.max(np.abs(o_last - o_nc)) <= 1e-13 and np.max(np.abs(l_last - l_nc)) <= 1e-13
+
+
 ALL_PINS = [
     pin_two_block_note, pin_four_scores_weights, pin_figure_7_9, pin_rows_of_p_sum_to_one,
     pin_causal_first_query, pin_uniform_scores, pin_constant_values, pin_key_shift,
     pin_key_permutation, pin_blockwise_equals_one_shot, pin_exact_summation,
     pin_library_forward, pin_library_backward, pin_finite_differences, pin_delta_identity,
-    pin_gqa_gradient_is_group_sum, pin_sampled_rows_match_full,
+    pin_gqa_gradient_is_group_sum, pin_sampled_rows_match_full, pin_query_offset_is_a_row_block,
 ]

@@ -113,3 +113,18 @@ def test_product_path_never_touches_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def fwd_ex(lib, Nq=16, Nk=64, off=48, d=64, causal=1, q=P):
+    return lib.fa_forward_ex(q, P, P, P, P, 1, 2, 1, Nq, Nk, d, ctypes.c_float(0.125), causal,
+                             off, None)
+
+
+@pytest.mark.parametrize("kw", [dict(off=-1), dict(Nk=0), dict(Nq=0), dict(q=Q), dict(causal=3),
+                                dict(off=2**31 - 10)])
+def test_forward_ex_rejects_invalid_arguments(lib, kw):
+    assert fwd_ex(lib, **kw) == fa.FA_ERR_INVALID_ARGUMENT
+
+
+def test_forward_ex_rejects_unsupported_head_dim(lib):
+    assert fwd_ex(lib, d=32) == fa.FA_ERR_UNSUPPORTED

@@ -116,3 +116,51 @@ def test_selftest_timeout_is_reported_and_device_stays_usable():
     assert fa.fa_last_device_error() == 0  # cleared
     w = WORKLOADS["single_head_n256"]
     forward_vs_oracle(workload_inputs(w), w.causal, w.scale)
+
+
+@pytest.mark.parametrize("Nq,Nk,off,causal,d,Hq,Hkv", [
+    (1, 70, 69, True, 64, 2, 2),        # one query against 70 positions (the decode case)
+    (1, 70, 0, True, 64, 2, 2),         # ... that sees only key 0
+    (1, 70, 69, False, 64, 2, 1),
+    (128, 1000, 872, True, 64, 4, 2),   # prefill continuing a cache
+    (300, 377, 77, True, 128, 2, 2),    # offset not a multiple of the tile
+    (257, 300, 0, True, 64, 2, 2),      # top-left alignment, N_q < N_kv
+    (100, 513, 413, False, 128, 4, 1),
+    (64, 4096, 4032, True, 128, 8, 2),
+])
+def test_query_offset_against_the_oracle(Nq, Nk, off, causal, d, Hq, Hkv):
+    import exact_attention_27_gb300 as fa
+    inp = make_inputs(1, Hq, Hkv, Nq, d, seed=Nq + Nk, Nk=Nk)
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o, lse = fa.attention_forward(q, k, v, causal=causal, scale=scale, q_offset=off)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == 0
+    o_ref, l_ref = oracle.attention_forward(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]),
+                                            scale, causal, q_offset=off)
+    check_forward(o, lse, o_ref, l_ref, f"offset {off}")
+
+
+def test_offset_rows_equal_rows_of_the_full_forward():
+    """Rows o..o+n-1 computed as queries with offset o match those rows of the
+    same-sequence causal forward bit for bit (each row's arithmetic is the same)."""
+    import exact_attention_27_gb300 as fa
+    inp = make_inputs(2, 4, 2, 700, 64, seed=77)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o_full, l_full = fa.attention_forward(q, k, v, causal=True, scale=0.125)
+    for off, n in ((0, 128), (100, 300), (699, 1), (513, 187)):
+        qs = q[:, :, off:off + n].contiguous()
+        o, lse = fa.attention_forward(qs, k, v, causal=True, scale=0.125, q_offset=off)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_full[:, :, off:off + n]), off
+        assert torch.equal(lse, l_full[:, :, off:off + n]), off
+
+
+def test_forward_ex_with_equal_lengths_is_forward():
+    import exact_attention_27_gb300 as fa
+    inp = make_inputs(1, 2, 2, 333, 128, seed=4)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o1, l1 = fa.attention_forward(q, k, v, causal=True)
+    o2, l2 = fa.attention_forward(q, k, v, causal=True, q_offset=0)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)

@@ -18,6 +18,9 @@ MUTATIONS = [
     ("max_not_subtracted", "s[j] = exp(s[j] - M);", "s[j] = exp(s[j]);"),
     ("mask_hides_diagonal", "if (causal && j > pos) {", "if (causal && j >= pos) {"),
     ("mask_leaks_next_key", "if (causal && j > pos) {", "if (causal && j > pos + 1) {"),
+    ("offset_ignored_forward",
+     "score_row(q_head + i * d, k_head, Nk, d, scale, causal, i + q_offset, P + r * Nk);",
+     "score_row(q_head + i * d, k_head, Nk, d, scale, causal, i, P + r * Nk);"),
     ("no_normalisation", "for (int64_t j = 0; j < Nk; ++j) s[j] /= Z;", ""),
     ("lse_without_max", "M + log(Z);", "log(Z);"),
     ("pv_uses_keys",
