@@ -18,7 +18,7 @@ import math
 from ._lib import FaError, library, status_string  # noqa: F401
 
 __all__ = [
-    "FaError", "fa_forward", "fa_forward_ex", "fa_backward", "fa_backward_preprocess", "fa_status_string",
+    "FaError", "fa_forward", "fa_forward_ex", "fa_backward", "fa_backward_deterministic", "fa_backward_preprocess", "fa_status_string",
     "fa_last_device_error", "fa_selftest_wait_timeout", "fa_set_backward_events", "attention_forward", "attention_backward",
     "library",
 ]
@@ -115,6 +115,20 @@ def fa_backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, stream=None):
                                  int(bool(causal)), _stream(stream)), "fa_backward")
 
 
+def fa_backward_deterministic(q, k, v, o, lse, do, dq, dk, dv, scale, causal, stream=None):
+    """fa_backward_deterministic of include/fa.h: bit-reproducible gradients."""
+    B, Hq, Hkv, N, d = _shapes(q, k)
+    for name, t, shp in (("q", q, None), ("k", k, None), ("v", v, k.shape), ("o", o, q.shape),
+                         ("do", do, q.shape), ("dq", dq, q.shape), ("dk", dk, k.shape),
+                         ("dv", dv, k.shape)):
+        _bf16_cuda(name, t, shp)
+    _f32_cuda("lse", lse, (B, Hq, N))
+    _check(library().fa_backward_deterministic(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, ctypes.c_float(scale),
+        int(bool(causal)), _stream(stream)), "fa_backward_deterministic")
+
+
 def fa_backward_preprocess(o, do, D, stream=None):
     """fa_backward_preprocess of include/fa.h: D[r] = sum_c dO[r, c] O[r, c]."""
     _bf16_cuda("o", o)
@@ -162,13 +176,16 @@ def attention_forward(q, k, v, causal=False, scale=None, q_offset=None, stream=N
     return o, lse
 
 
-def attention_backward(q, k, v, o, lse, do, causal=False, scale=None, stream=None):
-    """Allocates dq, dk, dv on q's device and runs fa_backward; returns them."""
+def attention_backward(q, k, v, o, lse, do, causal=False, scale=None, deterministic=False,
+                       stream=None):
+    """Allocates dq, dk, dv on q's device and runs fa_backward (or
+    fa_backward_deterministic); returns them."""
     import torch
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    fa_backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, stream)
+    run = fa_backward_deterministic if deterministic else fa_backward
+    run(q, k, v, o, lse, do, dq, dk, dv, scale, causal, stream)
     return dq, dk, dv

@@ -41,6 +41,8 @@ def _declare(lib):
     lib.fa_forward_ex.argtypes = [p, p, p, p, p, i, i, i, i, i, i, f, i, i, p]
     lib.fa_backward.restype = i
     lib.fa_backward.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, p]
+    lib.fa_backward_deterministic.restype = i
+    lib.fa_backward_deterministic.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, p]
     lib.fa_backward_noalloc.restype = i
     lib.fa_backward_noalloc.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, p]
     lib.fa_backward_preprocess.restype = i

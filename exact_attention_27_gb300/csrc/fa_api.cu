@@ -226,6 +226,39 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   return (e == cudaSuccess && ef == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_backward_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dO, void* dq, void* dk,
+                                    void* dv, int B, int H_q, int H_kv, int N, int d, float scale,
+                                    int causal, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
+  const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
+  for (const void* p : p16)
+    if (!aligned16(p)) return FA_ERR_INVALID_ARGUMENT;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_INVALID_ARGUMENT;
+  uint32_t* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  const long long rows = static_cast<long long>(B) * H_q * N;
+  void* scratch = nullptr;
+  if (cudaMallocAsync(&scratch, static_cast<size_t>(rows) * sizeof(float), stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+  float* Dbuf = static_cast<float*>(scratch);
+  fa::BwdMaps m{};
+  const bool ok = make_map_bf16(&m.q, q, d, N, static_cast<long long>(B) * H_q) &&
+                  make_map_bf16(&m.k, k, d, N, static_cast<long long>(B) * H_kv) &&
+                  make_map_bf16(&m.v, v, d, N, static_cast<long long>(B) * H_kv) &&
+                  make_map_bf16(&m.dO, dO, d, N, static_cast<long long>(B) * H_q);
+  fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
+  cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
+  if (e == cudaSuccess) e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream);
+  if (e == cudaSuccess)
+    e = fa::launch_backward(m, lse, Dbuf, nullptr, dk, dv, s, err, stream, /*with_dq=*/false);
+  if (e == cudaSuccess) e = fa::launch_backward_dq(m, lse, Dbuf, dq, s, err, stream);
+  const cudaError_t ef = cudaFreeAsync(scratch, stream);
+  return (e == cudaSuccess && ef == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
+}
+
 const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "ok";

@@ -146,7 +146,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-template <int D, bool CAUSAL>
+// DQ = false builds the dK/dV-only kernel of the deterministic backward.
+template <int D, bool CAUSAL, bool DQ>
 __global__ void __launch_bounds__(192, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         // dQ_i = dS K_j    (A = dS: the dS^T buffer read MN-major; B = K_j MN-major)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
+        for (int kk = 0; kk < (DQ ? 8 : 0); ++kk)
           mma_ss(tmem + C::COL_DQ, smem_desc_sw128(sDS + kk * 2048, C::SUB_BYTES, 1024),
                  smem_desc_sw128(sK + kk * 2048, C::SUB_BYTES, 1024), id_q, kk > 0 ? 1u : 0u);
         mma_commit(bar(C::B_QDEMPTY + st));
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int pass = 0; pass < D / 64; ++pass) {
+      for (int pass = 0; pass < (DQ ? D / 64 : 0); ++pass) {
         if (t == 0) bulk_wait_group_read0();  // staging free again
         if (!(ok = wg_sync())) break;
         uint32_t a[32], bb[32];
@@ -479,11 +480,11 @@ cudaError_t launch_dq_finalize(const float* dq_acc, void* dq, long long n, float
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DQ>
 cudaError_t launch_bwd_t(const BwdMaps& m, const float* lse, const float* Dv, void* dk, void* dv,
                          const AttnShape& s, uint32_t* err, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  auto kern = fa_bwd_kernel<D, CAUSAL>;
+  auto kern = fa_bwd_kernel<D, CAUSAL, DQ>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -507,10 +508,14 @@ cudaError_t launch_bwd_t(const BwdMaps& m, const float* lse, const float* Dv, vo
 }
 
 cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* Dv, float*, void* dk,
-                            void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream) {
-  if (s.d == 64) return launch_backward_d64(m, lse, Dv, dk, dv, s, err, stream);
-  return s.causal ? launch_bwd_t<128, true>(m, lse, Dv, dk, dv, s, err, stream)
-                  : launch_bwd_t<128, false>(m, lse, Dv, dk, dv, s, err, stream);
+                            void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream,
+                            bool with_dq) {
+  if (s.d == 64) return launch_backward_d64(m, lse, Dv, dk, dv, s, err, stream, with_dq);
+  if (with_dq)
+    return s.causal ? launch_bwd_t<128, true, true>(m, lse, Dv, dk, dv, s, err, stream)
+                    : launch_bwd_t<128, false, true>(m, lse, Dv, dk, dv, s, err, stream);
+  return s.causal ? launch_bwd_t<128, true, false>(m, lse, Dv, dk, dv, s, err, stream)
+                  : launch_bwd_t<128, false, false>(m, lse, Dv, dk, dv, s, err, stream);
 }
 
 }  // namespace fa

@@ -76,7 +76,9 @@ struct Cfg64 {
   static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ drained (4 warp arrivals)
   static constexpr int B_WG = B_DQFREE + 1;       // drain-warpgroup internal sync (4 warp arrivals)
   static constexpr int B_LDFULL = B_WG + 1;       // [NLD] L/D slot filled (4 warp arrivals)
-  static constexpr int B_DRAIN = B_LDFULL + NLD;
+  static constexpr int B_LDEMPTY = B_LDFULL + NLD; // [NLD] L/D slot read (8 warp arrivals)
+  static constexpr int B_FINAL = B_LDEMPTY + NLD;  // every MMA issued has completed (once)
+  static constexpr int B_DRAIN = B_FINAL + 1;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -118,7 +120,10 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
-template <bool CAUSAL>
+// DQ = false builds the dK/dV-only kernel of the deterministic backward: no
+// dQ product, no dQ drain and no dS^T in shared memory; the per-tile
+// completion barrier still paces the L/D ring.
+template <bool CAUSAL, bool DQ>
 __global__ void __launch_bounds__(448, 1)
     fa_bwd64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV,
@@ -161,7 +166,11 @@ __global__ void __launch_bounds__(448, 1)
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQFREE), 4);
     mbar_init(bar(C::B_WG), 4);
-    for (int s = 0; s < C::NLD; ++s) mbar_init(bar(C::B_LDFULL + s), 4);
+    for (int s = 0; s < C::NLD; ++s) {
+      mbar_init(bar(C::B_LDFULL + s), 4);
+      mbar_init(bar(C::B_LDEMPTY + s), 8);
+    }
+    mbar_init(bar(C::B_FINAL), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -282,7 +291,7 @@ __global__ void __launch_bounds__(448, 1)
         // Queue the next S^T/dP^T before possibly waiting for the dQ drain, so
         // that the tensor core keeps working meanwhile.
         if (h + 2 < n_half && !issue_sdp(h + 2)) break;
-        if (a == 1) {
+        if (a == 1 && DQ) {
           if (s > 0) {
             if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma))
               break;
@@ -297,6 +306,10 @@ __global__ void __launch_bounds__(448, 1)
           mma_commit(bar(C::B_DQFULL));
           mma_commit(bar(C::B_DSFREE + (s & 1)));
         }
+        // Once, after the last half: everything issued has completed.  (A
+        // barrier that completes once per tile could not tell its last phase
+        // apart from an earlier one by parity when nothing holds it back.)
+        if (h == n_half - 1) mma_commit(bar(C::B_FINAL));
       }
       if (*abort_flag) {
         mma_commit(bar(C::B_DRAIN));
@@ -320,7 +333,7 @@ __global__ void __launch_bounds__(448, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SDP + a), (h >> 1) & 1, abort_flag, p.err,
                                              kErrTimeoutSoftmax));
       if (!ok) break;
-      if (s >= 2 && a == 0) {  // the dS^T buffer of tile s - 2 must have been read by its dQ MMA
+      if (DQ && s >= 2 && a == 0) {  // the dS^T buffer of tile s - 2 must have been read by its dQ MMA
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DSFREE + (s & 1)), ((s - 2) >> 1) & 1,
                                                abort_flag, p.err, kErrTimeoutSoftmax));
         if (!ok) break;
@@ -366,16 +379,19 @@ __global__ void __launch_bounds__(448, 1)
       }
       tmem_st16(sbuf, pk);         // P^T over this warpgroup's S^T columns
       tmem_st16(sbuf + 64, dk16);  // dS^T over its dP^T columns
-      // dS^T row t, queries 32wg .. 32wg+31 of the half: chunks 4wg..4wg+3 of block a.
-      const uint32_t ds_blk = sDS + (s & 1) * C::DS_BYTES + a * C::TILE;
+      if (DQ) {
+        // dS^T row t, queries 32wg .. 32wg+31 of the half: chunks 4wg..4wg+3 of block a.
+        const uint32_t ds_blk = sDS + (s & 1) * C::DS_BYTES + a * C::TILE;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-        st_shared_v4(ds_blk + sw128(t, wg * 4 + q4), dk16[4 * q4], dk16[4 * q4 + 1],
-                     dk16[4 * q4 + 2], dk16[4 * q4 + 3]);
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(ds_blk + sw128(t, wg * 4 + q4), dk16[4 * q4], dk16[4 * q4 + 1],
+                       dk16[4 * q4 + 2], dk16[4 * q4 + 3]);
+      }
       tmem_wait_st();
-      fence_proxy_async_smem();
+      if (DQ) fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive_warp(bar(C::B_PDS + a));
+      mbar_arrive_warp(bar(C::B_LDEMPTY + h % C::NLD));  // this half's L/D are no longer read
     }
   } else if (wg == 2) {
     // ------------------------------------------------------------ K/V -> TMEM, dQ drain, epilogue
@@ -427,15 +443,16 @@ __global__ void __launch_bounds__(448, 1)
       reinterpret_cast<float*>(smem + C::OFF_LD)[(h % C::NLD) * 128 + t] = val;
       mbar_arrive_warp(bar(C::B_LDFULL + h % C::NLD));
     };
-    // Halves of tiles 0..2 first; after draining tile s, the halves of tile
-    // s + 3 (their slots held tile s, whose halves are done by then).  The
-    // loads for tile s + 3 are issued before waiting for tile s.
+    // Halves of tiles 0..2 first; then, once the compute warps have read the
+    // slots of tile s, the halves of tile s + 3 go into them.  The loads for
+    // tile s + 3 are issued before waiting for tile s.
     for (int h = 0; h < C::NLD; ++h) store_ld(h, load_ld(h));
     for (int s = 0; ok && s < n_steps; ++s) {
       int bhq, it;
       step_coords(s, bhq, it);
       const float ld_next0 = load_ld(2 * (s + 3));
       const float ld_next1 = load_ld(2 * (s + 3) + 1);
+      if (DQ) {
       ok = __all_sync(0xffffffffu,
                       mbar_wait(bar(C::B_DQFULL), s & 1, abort_flag, p.err, kErrTimeoutOther));
       if (!ok) break;
@@ -461,14 +478,23 @@ __global__ void __launch_bounds__(448, 1)
         tma_reduce_add_3d(&tmdQ, sSTG + C::TILE, 32, it * C::BQ, bhq);
         bulk_commit_group();
       }
-      // dQ of tile s in TMEM means both halves of tile s were consumed, so the
-      // ring slots of tile s can take tile s + 3.
-      store_ld(2 * (s + 3), ld_next0);
-      store_ld(2 * (s + 3) + 1, ld_next1);
+      }  // DQ
+      // The ring slots of tile s take tile s + 3 once both halves of tile s
+      // were read (a barrier per slot, so that the refills cannot run ahead).
+      for (int x = 0; x < 2 && 2 * (s + 3) + x < n_half; ++x) {
+        const int h = 2 * s + x;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_LDEMPTY + h % C::NLD), (h / C::NLD) & 1,
+                                               abort_flag, p.err, kErrTimeoutOther));
+        if (!ok) break;
+        store_ld(2 * (s + 3) + x, x == 0 ? ld_next0 : ld_next1);
+      }
+      if (!ok) break;
     }
     if (t == 0) bulk_wait_group0();
     __syncwarp();  // lane 0 waited alone; the TMEM loads below are warp-collective
-    // ---- epilogue: every MMA has completed once the last dQ was seen
+    // ---- epilogue, once every MMA has completed
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_FINAL), 0, abort_flag, p.err,
+                                                   kErrTimeoutEpilogue));
     if (ok) {
       tc_fence_after();
       const int key = jt * C::BK + t;
@@ -513,11 +539,11 @@ __global__ void __launch_bounds__(448, 1)
   }
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool DQ>
 cudaError_t launch_t(const BwdMaps& m, const float* lse, const float* Dv, void* dk, void* dv,
                      const AttnShape& s, uint32_t* err, cudaStream_t stream) {
   using C = Cfg64;
-  auto kern = fa_bwd64_kernel<CAUSAL>;
+  auto kern = fa_bwd64_kernel<CAUSAL, DQ>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -545,9 +571,13 @@ cudaError_t launch_t(const BwdMaps& m, const float* lse, const float* Dv, void* 
 }  // namespace
 
 cudaError_t launch_backward_d64(const BwdMaps& m, const float* lse, const float* Dv, void* dk,
-                                void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream) {
-  return s.causal ? launch_t<true>(m, lse, Dv, dk, dv, s, err, stream)
-                  : launch_t<false>(m, lse, Dv, dk, dv, s, err, stream);
+                                void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream,
+                                bool with_dq) {
+  if (with_dq)
+    return s.causal ? launch_t<true, true>(m, lse, Dv, dk, dv, s, err, stream)
+                    : launch_t<false, true>(m, lse, Dv, dk, dv, s, err, stream);
+  return s.causal ? launch_t<true, false>(m, lse, Dv, dk, dv, s, err, stream)
+                  : launch_t<false, false>(m, lse, Dv, dk, dv, s, err, stream);
 }
 
 }  // namespace fa

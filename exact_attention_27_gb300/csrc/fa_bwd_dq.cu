@@ -1,0 +1,365 @@
+// dQ kernel of the deterministic backward pass on sm_103a.
+//
+// "L'attention fusionnee", section "La passe arriere : recalculer plutot que
+// garder", describes two kernels instead of one: one for dK and dV, and one
+// for dQ that walks the key tiles in the forward pass's order.  It recomputes
+// S and dP (three products more than the single kernel) but needs no atomic
+// addition, so the result does not depend on the order in which the GPU runs
+// its blocks and repeated runs give identical bits.  This is the dQ kernel.
+//
+// One CTA owns 128 query rows of one (batch, query head), like the forward:
+//   S_j  = Q K_j^T            tcgen05.mma, operands in shared memory
+//   dP_j = dO V_j^T           tcgen05.mma
+//   P    = exp2(S scale log2e - L log2e), dS = P o (dP - D)   one thread per row
+//   dQ  += dS K_j             tcgen05.mma, A = dS (bf16) from tensor memory
+// and at the end dq = bf16(scale dQ).  Under the causal mask query tile i
+// visits key tiles 0..i only (tiles wholly in the future are skipped).
+//
+// Warps: 0-3 one query row per thread, 4 TMA producer, 5 MMA issuer.
+// Tensor memory: S [0,128) (dS as bf16 over its first 64 columns),
+// dP [128,256), dQ [256, 256+D).
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct DqCfg {
+  static constexpr int BM = 128;                 // query rows per CTA
+  static constexpr int BN = 128;                 // keys per tile
+  static constexpr int SUB = D / 64;
+  static constexpr int SUB_BYTES = 128 * 128;
+  static constexpr int TILE = SUB * SUB_BYTES;   // 128 x D bf16
+  static constexpr int NS = (D == 64) ? 4 : 2;   // K/V ring stages
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = OFF_Q + TILE;
+  static constexpr int OFF_K = OFF_DO + TILE;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  static constexpr int B_QD = 0;
+  static constexpr int B_KFULL = 1;
+  static constexpr int B_KEMPTY = B_KFULL + NS;
+  static constexpr int B_VFULL = B_KEMPTY + NS;
+  static constexpr int B_VEMPTY = B_VFULL + NS;
+  static constexpr int B_SFULL = B_VEMPTY + NS;   // S and dP of a tile in TMEM
+  static constexpr int B_DSREADY = B_SFULL + 1;   // dS in TMEM (4 warp arrivals)
+  static constexpr int B_DQDONE = B_DSREADY + 1;  // every dQ MMA done (completes once)
+  static constexpr int B_DRAIN = B_DQDONE + 1;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
+};
+
+struct DqParams {
+  const float* lse;
+  const float* Dvec;
+  __nv_bfloat16* dq;
+  int N, Hq, G, n_qtiles, n_ktiles, n_heads, heads_per_group;
+  float scale;
+  float scale_log2;
+  uint32_t* err;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmdO, const DqParams p) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  // Same launch order as the forward: groups of heads, heaviest tiles first.
+  const int per_group = p.heads_per_group * p.n_qtiles;
+  const int grp = static_cast<int>(blockIdx.x) / per_group;
+  const int rem = static_cast<int>(blockIdx.x) - grp * per_group;
+  const int in_grp = min(p.heads_per_group, p.n_heads - grp * p.heads_per_group);
+  const int qi_ = rem / in_grp;
+  const int bh = grp * p.heads_per_group + (rem - qi_ * in_grp);
+  const int qt = CAUSAL ? (p.n_qtiles - 1 - qi_) : qi_;
+  const int b = bh / p.Hq;
+  const int hq = bh - b * p.Hq;
+  const int kvz = b * (p.Hq / p.G) + hq / p.G;
+  const int n_kv = CAUSAL ? min(qt + 1, p.n_ktiles) : p.n_ktiles;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_QD), 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(bar(C::B_KFULL + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 1);
+      mbar_init(bar(C::B_VFULL + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), 1);
+    }
+    mbar_init(bar(C::B_SFULL), 1);
+    mbar_init(bar(C::B_DSREADY), 4);
+    mbar_init(bar(C::B_DQDONE), 1);
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t sQ = sbase + C::OFF_Q;
+  const uint32_t sdO = sbase + C::OFF_DO;
+  const uint32_t sK = sbase + C::OFF_K;
+  const uint32_t sV = sbase + C::OFF_V;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(bar(C::B_QD), 2 * C::TILE);
+#pragma unroll
+      for (int s = 0; s < C::SUB; ++s) {
+        tma_load_3d(sQ + s * C::SUB_BYTES, &tmQ, bar(C::B_QD), 64 * s, qt * C::BM, bh);
+        tma_load_3d(sdO + s * C::SUB_BYTES, &tmdO, bar(C::B_QD), 64 * s, qt * C::BM, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % C::NS;
+        const uint32_t ph = ((j / C::NS) - 1) & 1;
+        if (j >= C::NS &&
+            !mbar_wait(bar(C::B_KEMPTY + st), ph, abort_flag, p.err, kErrTimeoutLoad))
+          break;
+        mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE);
+#pragma unroll
+        for (int s = 0; s < C::SUB; ++s)
+          tma_load_3d(sK + st * C::TILE + s * C::SUB_BYTES, &tmK, bar(C::B_KFULL + st), 64 * s,
+                      j * C::BN, kvz);
+        if (j >= C::NS &&
+            !mbar_wait(bar(C::B_VEMPTY + st), ph, abort_flag, p.err, kErrTimeoutLoad))
+          break;
+        mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE);
+#pragma unroll
+        for (int s = 0; s < C::SUB; ++s)
+          tma_load_3d(sV + st * C::TILE + s * C::SUB_BYTES, &tmV, bar(C::B_VFULL + st), 64 * s,
+                      j * C::BN, kvz);
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        mbar_wait_timed(bar(C::B_QD), 0);
+        for (int j = max(0, issued - C::NS); j < issued; ++j) {
+          mbar_wait_timed(bar(C::B_KFULL + j % C::NS), (j / C::NS) & 1);
+          mbar_wait_timed(bar(C::B_VFULL + j % C::NS), (j / C::NS) & 1);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);  // S, dP
+      constexpr uint32_t ID_Q = idesc_bf16_f32(128, D, false, true);     // dQ (B = K MN-major)
+      const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t do_desc = smem_desc_sw128(sdO, 16, 1024);
+      const uint64_t k_kmaj = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t v_kmaj = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t k_mn = smem_desc_sw128(sK, C::SUB_BYTES, 1024);
+      bool ok = mbar_wait(bar(C::B_QD), 0, abort_flag, p.err, kErrTimeoutMma);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % C::NS;
+        if (!mbar_wait(bar(C::B_KFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
+          break;
+        tc_fence_after();
+        const uint64_t kd = desc_add(k_kmaj, st * C::TILE);
+        mma_ss_k<ID_S, 0>(tmem + C::COL_S, q_desc, kd);
+#pragma unroll
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+          mma_ss_k<ID_S, 1>(tmem + C::COL_S, desc_add(q_desc, off), desc_add(kd, off));
+        }
+        if (!mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
+          break;
+        tc_fence_after();
+        const uint64_t vd = desc_add(v_kmaj, st * C::TILE);
+        mma_ss_k<ID_S, 0>(tmem + C::COL_DP, do_desc, vd);
+#pragma unroll
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+          mma_ss_k<ID_S, 1>(tmem + C::COL_DP, desc_add(do_desc, off), desc_add(vd, off));
+        }
+        mma_commit(bar(C::B_SFULL));
+        mma_commit(bar(C::B_VEMPTY + st));
+        if (!mbar_wait(bar(C::B_DSREADY), j & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+        tc_fence_after();
+        // dQ += dS K_j: dS packed in S's first 64 columns, 16 keys = 8 columns per step;
+        // K_j read MN-major, 16 key rows (2 KB) per step.
+        const uint64_t kmn = desc_add(k_mn, st * C::TILE);
+        if (j == 0)
+          mma_ts_k<ID_Q, 0>(tmem + C::COL_DQ, tmem + C::COL_S, kmn);
+        else
+          mma_ts_k<ID_Q, 1>(tmem + C::COL_DQ, tmem + C::COL_S, kmn);
+#pragma unroll
+        for (int kk = 1; kk < 8; ++kk)
+          mma_ts_k<ID_Q, 1>(tmem + C::COL_DQ, tmem + C::COL_S + kk * 8,
+                            desc_add(kmn, kk * 2048));
+        mma_commit(bar(C::B_KEMPTY + st));
+        // Once, after the last tile: a barrier that completed once per tile
+        // could not tell its last phase from an earlier one by parity alone.
+        if (j == n_kv - 1) mma_commit(bar(C::B_DQDONE));
+      }
+      if (*abort_flag) {
+        mma_commit(bar(C::B_DRAIN));
+        mbar_wait_timed(bar(C::B_DRAIN), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ query rows
+    const int row = threadIdx.x;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int qi = qt * C::BM + row;
+    const bool live = qi < p.N;
+    const size_t ridx = static_cast<size_t>(bh) * p.N + (live ? qi : 0);
+    const float L2 = live ? p.lse[ridx] * kLog2e : INFINITY;  // dead rows: P = 0
+    const float Drow = live ? p.Dvec[ridx] : 0.0f;
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL), j & 1, abort_flag, p.err,
+                                             kErrTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after();
+      const int kbase = j * C::BN;
+      const bool need_mask = __any_sync(
+          0xffffffffu, (kbase + C::BN > p.N) || (CAUSAL && kbase + C::BN - 1 > qt * C::BM));
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(tmem + lane_off + C::COL_S + cc * 32, sv);
+        tmem_ld32(tmem + lane_off + C::COL_DP + cc * 32, dpv);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float pr = ex2_approx(fmaf(__uint_as_float(sv[2 * u + e]), c, -L2));
+            if (need_mask) {
+              const int key = kbase + cc * 32 + 2 * u + e;
+              if (key >= p.N || (CAUSAL && key > qi)) pr = 0.0f;
+            }
+            ds[e] = pr * (__uint_as_float(dpv[2 * u + e]) - Drow);
+          }
+          pk[u] = pack_bf16x2(ds[0], ds[1]);
+        }
+        // dS (bf16) over S columns already read: keys cc*32.. -> columns cc*16..
+        tmem_st16(tmem + lane_off + C::COL_S + cc * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_warp(bar(C::B_DSREADY));
+    }
+    // ---- epilogue: dq = bf16(scale dQ), one row per thread
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQDONE), 0, abort_flag, p.err,
+                                                   kErrTimeoutEpilogue));
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* qrow = p.dq + ridx * D;
+#pragma unroll
+      for (int q4 = 0; q4 < D / 32; ++q4) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::COL_DQ + q4 * 32, r);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          pk[u] = pack_bf16x2(__uint_as_float(r[2 * u]) * p.scale,
+                              __uint_as_float(r[2 * u + 1]) * p.scale);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(qrow + q4 * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+    }
+  }
+
+  // Every warp reconverges first: in the TMA and MMA warps only one lane did
+  // the work, and the CTA barrier below must count whole, converged warps.
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dq_t(const BwdMaps& m, const float* lse, const float* Dv, void* dq,
+                        const AttnShape& s, uint32_t* err, cudaStream_t stream) {
+  using C = DqCfg<D>;
+  auto kern = fa_bwd_dq_kernel<D, CAUSAL>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  DqParams p;
+  p.lse = lse;
+  p.Dvec = Dv;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.N = s.N;
+  p.Hq = s.Hq;
+  p.G = s.Hq / s.Hkv;
+  p.n_qtiles = (s.N + C::BM - 1) / C::BM;
+  p.n_ktiles = (s.N + C::BN - 1) / C::BN;
+  p.n_heads = s.B * s.Hq;
+  {
+    const double kv_bytes = 2.0 * s.N * D * 2.0;
+    long long kv_heads = static_cast<long long>(48.0 * 1024 * 1024 / kv_bytes);
+    if (kv_heads < 1) kv_heads = 1;
+    long long hpg = kv_heads * p.G;
+    if (hpg > p.n_heads) hpg = p.n_heads;
+    p.heads_per_group = static_cast<int>(hpg);
+  }
+  p.scale = s.scale;
+  p.scale_log2 = s.scale * kLog2e;
+  p.err = err;
+  const long long grid = static_cast<long long>(p.n_heads) * p.n_qtiles;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dO,
+                                                                         p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward_dq(const BwdMaps& m, const float* lse, const float* Dv, void* dq,
+                               const AttnShape& s, uint32_t* err, cudaStream_t stream) {
+  if (s.d == 64)
+    return s.causal ? launch_dq_t<64, true>(m, lse, Dv, dq, s, err, stream)
+                    : launch_dq_t<64, false>(m, lse, Dv, dq, s, err, stream);
+  return s.causal ? launch_dq_t<128, true>(m, lse, Dv, dq, s, err, stream)
+                  : launch_dq_t<128, false>(m, lse, Dv, dq, s, err, stream);
+}
+
+}  // namespace fa

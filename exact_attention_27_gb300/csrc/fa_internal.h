@@ -34,12 +34,20 @@ struct BwdMaps {
 };
 
 // Head dimension 64 (fa_bwd_d64.cu); launch_backward dispatches to it.
+// with_dq = false: dK and dV only (the first kernel of the deterministic
+// backward; dq_acc and the dq_acc map are not used).
 cudaError_t launch_backward_d64(const BwdMaps& m, const float* lse, const float* D, void* dk,
-                                void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream);
+                                void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream,
+                                bool with_dq);
 
 cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* D, float* dq_acc,
                             void* dk, void* dv, const AttnShape& s, uint32_t* err,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool with_dq = true);
+
+// dQ of the deterministic backward (fa_bwd_dq.cu): per query tile, key tiles
+// in forward order, dq = bf16(scale * dS K) written directly, no atomics.
+cudaError_t launch_backward_dq(const BwdMaps& m, const float* lse, const float* D, void* dq,
+                               const AttnShape& s, uint32_t* err, cudaStream_t stream);
 
 // Helpers defined in fa_api.cu for other translation units: the per-device
 // error word the kernels' bounded waits report into, and tensor-map encoding

@@ -122,6 +122,23 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       cudaStream_t stream);
 
 /*
+ * Backward pass whose results are bit-for-bit reproducible from run to run.
+ * Source: "L'attention fusionnee", section "La passe arriere : recalculer
+ * plutot que garder": instead of one kernel that adds each key tile's share
+ * of dQ with atomic additions, one kernel computes dK and dV and a second
+ * computes dQ, walking the key tiles in the forward pass's order; it redoes
+ * three products but needs no atomics, so the result does not depend on the
+ * order in which the GPU runs its blocks.
+ *
+ * Arguments, layouts, outputs and return codes are those of fa_backward.
+ * Scratch: only D (B*H_q*N*4 bytes), taken and released stream-ordered.
+ */
+fa_status fa_backward_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dO, void* dq, void* dk,
+                                    void* dv, int B, int H_q, int H_kv, int N, int d, float scale,
+                                    int causal, cudaStream_t stream);
+
+/*
  * Scratch reserved by the library for fa_backward_noalloc, in bytes (32 MiB).
  */
 #define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
