@@ -6,20 +6,28 @@
 // mai scrivere la matrice": the query block stays, K_j / V_j blocks move, the
 // S_ij tile is B_r x B_c, here 128 x 128).
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t of the tile.  Online
-//              softmax per key tile, rescale of the O accumulator, epilogue.
-//   warp 4     TMA producer: Q once, then K_j and V_j into a ring of stages.
-//   warp 5     MMA issuer (one thread) and TMEM owner:
-//                S_j = Q K_j^T           (tcgen05.mma, A and B from shared memory)
-//                O  += P_j V_j           (tcgen05.mma, A = P from tensor memory)
+// Each CTA owns two consecutive query tiles (A and B) and keeps one softmax
+// warpgroup per tile, so that one tile's softmax runs while the tensor core
+// works on the other tile's products (a ping-pong between the two).
+//
+// Warp roles (384 threads, three warpgroups):
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread t owns
+//              query row t of its tile.  Online softmax per key tile, rescale
+//              of the O accumulator, epilogue.
+//   warp 8     TMA producer: both Q tiles once, then K_j and V_j into a ring.
+//   warps 10-11 idle (they complete the third warpgroup)
+//   warp 9     MMA issuer (one thread) and TMEM owner, in the order
+//              S_A(0) S_B(0), then per key tile j:
+//              O_A += P_A V_j, S_A(j+1) = Q_A K_{j+1}^T, O_B += P_B V_j, S_B(j+1)
+//              (S: A and B from shared memory; O: A = P from tensor memory).
+// Registers: launched at 168 per thread; the third warpgroup gives most of
+// its share to the two softmax warpgroups (56 / 224 / 224: 128 x (224 + 224
+// + 56) = 384 x 168, the launch total).
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
-//   columns   0..127  S buffer 0     (P_j as packed bf16 overwrites columns 0..63)
-//   columns 128..255  S buffer 1
-//   columns 256..256+D-1  O accumulator (fp32)
-// Two S buffers let the tensor core compute S_{j+1} while the softmax warps
-// work on S_j.
+//   columns   0..127  S of tile A    (P as packed bf16 overwrites columns 0..63)
+//   columns 128..255  S of tile B
+//   columns 256..256+2D-1  O accumulators of tiles A and B (fp32)
 //
 // Online softmax ("L'attention fusionnee", section "Le softmax en ligne"):
 // per key tile m' = max(m, max s), p = exp(s - m'), l = l e^(m - m') + sum p,
@@ -63,9 +71,9 @@ struct FwdCfg {
   static constexpr int SUB = D / 64;             // 128-byte column blocks per row
   static constexpr int SUB_BYTES = 128 * 128;    // one 128-row x 64-col bf16 block
   static constexpr int TILE = SUB * SUB_BYTES;   // one 128 x D bf16 tile
-  static constexpr int NS = (D == 64) ? 4 : 3;   // K/V ring stages
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE;
+  static constexpr int NS = (D == 64) ? 4 : 2;   // K/V ring stages
+  static constexpr int OFF_Q = 0;                // two query tiles
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_BAR = OFF_V + NS * TILE;
   // barrier slots
@@ -74,16 +82,16 @@ struct FwdCfg {
   static constexpr int B_KEMPTY = B_KFULL + NS;
   static constexpr int B_VFULL = B_KEMPTY + NS;
   static constexpr int B_VEMPTY = B_VFULL + NS;
-  static constexpr int B_SFULL = B_VEMPTY + NS;  // 2
-  static constexpr int B_PFULL = B_SFULL + 2;    // 2
-  static constexpr int B_ODONE = B_PFULL + 2;
-  static constexpr int B_DRAIN = B_ODONE + 1;    // abort path: MMAs in flight
+  static constexpr int B_SFULL = B_VEMPTY + NS;  // [2] per query tile
+  static constexpr int B_PFULL = B_SFULL + 2;    // [2] per query tile (4 warp arrivals)
+  static constexpr int B_ODONE = B_PFULL + 2;    // [2] per query tile
+  static constexpr int B_DRAIN = B_ODONE + 2;    // abort path: MMAs in flight
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort word
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O = 256;
+  static constexpr uint32_t COL_O = 256;         // O of tile x at 256 + x * D
 };
 
 struct FwdParams {
@@ -95,6 +103,7 @@ struct FwdParams {
   int Hq;
   int G;          // query heads per key/value head
   int n_qtiles;
+  int n_qpairs;   // CTAs per head: two query tiles each
   int n_ktiles;
   int n_heads;          // B * Hq
   int heads_per_group;  // launch-order grouping, a multiple of G
@@ -103,7 +112,7 @@ struct FwdParams {
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
@@ -118,19 +127,27 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5;
   // Launch order: heads are taken in groups of p.heads_per_group (sized on
   // the host so that the group's K/V fits comfortably in L2); within a group
-  // the heaviest causal query tiles of all its heads come first.
-  const int per_group = p.heads_per_group * p.n_qtiles;
+  // the heaviest causal query-tile pairs of all its heads come first.
+  const int per_group = p.heads_per_group * p.n_qpairs;
   const int grp = static_cast<int>(blockIdx.x) / per_group;
   const int rem = static_cast<int>(blockIdx.x) - grp * per_group;
   const int in_grp = min(p.heads_per_group, p.n_heads - grp * p.heads_per_group);
-  const int qi_ = rem / in_grp;
-  const int bh = grp * p.heads_per_group + (rem - qi_ * in_grp);  // flattened (batch, query head)
-  const int qt = CAUSAL ? (p.n_qtiles - 1 - qi_) : qi_;
+  const int pi_ = rem / in_grp;
+  const int bh = grp * p.heads_per_group + (rem - pi_ * in_grp);  // flattened (batch, query head)
+  const int pair = CAUSAL ? (p.n_qpairs - 1 - pi_) : pi_;
   const int b = bh / p.Hq;
   const int hq = bh - b * p.Hq;
   const int kvz = b * (p.Hq / p.G) + hq / p.G;  // flattened (batch, kv head)
-  const int n_kv =
-      CAUSAL ? min((p.q_offset + qt * C::BM + C::BM - 1) / C::BN + 1, p.n_ktiles) : p.n_ktiles;
+  // Key tiles visited by query tile 2*pair + x (0 if that tile is past N).
+  auto tiles_for = [&](int x) -> int {
+    const int qt = 2 * pair + x;
+    if (qt >= p.n_qtiles) return 0;
+    return CAUSAL ? min((p.q_offset + qt * C::BM + C::BM - 1) / C::BN + 1, p.n_ktiles)
+                  : p.n_ktiles;
+  };
+  const int nA = tiles_for(0);
+  const int nB = tiles_for(1);
+  const int n_kv = max(nA, nB);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_QFULL), 1);
@@ -140,16 +157,16 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(bar(C::B_VFULL + s), 1);
       mbar_init(bar(C::B_VEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::B_SFULL + s), 1);
-      mbar_init(bar(C::B_PFULL + s), 4);  // one arrival per softmax warp
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(C::B_SFULL + x), 1);
+      mbar_init(bar(C::B_PFULL + x), 4);  // one arrival per softmax warp of the tile
+      mbar_init(bar(C::B_ODONE + x), 1);
     }
-    mbar_init(bar(C::B_ODONE), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -162,17 +179,22 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sK = sbase + C::OFF_K;
   const uint32_t sV = sbase + C::OFF_V;
 
-  if (warp == 4) {
+  if (warp >= 8) {
+  reg_decrease<56>();
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       const uint64_t keep = policy_evict_last();  // K/V are re-read by the other query tiles
-      mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE);
+      mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE);
 #pragma unroll
-      for (int s = 0; s < C::SUB; ++s)
-        tma_load_3d(sQ + s * C::SUB_BYTES, &tmQ, bar(C::B_QFULL), 64 * s, qt * C::BM, bh);
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int s = 0; s < C::SUB; ++s)
+          tma_load_3d(sQ + x * C::TILE + s * C::SUB_BYTES, &tmQ, bar(C::B_QFULL), 64 * s,
+                      (2 * pair + x) * C::BM, bh);
       int issued = 0;  // K/V tiles whose loads were issued
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % C::NS;
@@ -204,57 +226,88 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // Order: S_A(0) S_B(0), then per key tile j: PV_A(j) S_A(j+1) PV_B(j)
+    // S_B(j+1), so that each tile's softmax overlaps the other tile's MMAs.
     if (elect_one()) {
       constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t ID_O = idesc_bf16_f32(128, D, false, true);
-      // Descriptors built once; k-steps move them by compile-time offsets.
       const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t k_desc = smem_desc_sw128(sK, 16, 1024);
       const uint64_t v_desc = smem_desc_sw128(sV, C::SUB_BYTES, 1024);
+      const int nx[2] = {nA, nB};
       bool ok = mbar_wait(bar(C::B_QFULL), 0, abort_flag, p.err, kErrTimeoutMma);
-      // S_j = Q K_j^T into S buffer j & 1; frees the K stage when done.
-      auto issue_s = [&](int j) -> bool {
+      // S_x(j) = Q_x K_j^T into tile x's S columns.
+      auto issue_s = [&](int x, int j) {
+        const uint32_t d_tmem = tmem + x * 128;
+        const uint64_t qd = desc_add(q_desc, x * C::TILE);
+        const uint64_t kd = desc_add(k_desc, (j % C::NS) * C::TILE);
+        mma_ss_k<ID_S, 0>(d_tmem, qd, kd);
+#pragma unroll
+        for (int kk = 1; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+          mma_ss_k<ID_S, 1>(d_tmem, desc_add(qd, off), desc_add(kd, off));
+        }
+        mma_commit(bar(C::B_SFULL + x));
+      };
+      // K_j is used by the S products of both tiles; wait for it once and
+      // release it after its last use.
+      auto issue_s_both = [&](int j) -> bool {
         const int st = j % C::NS;
         if (!mbar_wait(bar(C::B_KFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
           return false;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (j & 1) * 128;
-        const uint64_t kd = desc_add(k_desc, st * C::TILE);
-        mma_ss_k<ID_S, 0>(d_tmem, q_desc, kd);
-#pragma unroll
-        for (int kk = 1; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          mma_ss_k<ID_S, 1>(d_tmem, desc_add(q_desc, off), desc_add(kd, off));
-        }
-        mma_commit(bar(C::B_SFULL + (j & 1)));
-        mma_commit(bar(C::B_KEMPTY + st));
         return true;
       };
-      if (ok) ok = issue_s(0);
+      if (ok && n_kv > 0) {
+        ok = issue_s_both(0);
+        if (ok) {
+          if (nA > 0) issue_s(0, 0);
+          if (nB > 0) issue_s(1, 0);
+          mma_commit(bar(C::B_KEMPTY + 0));
+        }
+      }
       for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv && !issue_s(j + 1)) break;
-        const int sb = j & 1;
         const int st = j % C::NS;
-        if (!mbar_wait(bar(C::B_PFULL + sb), (j >> 1) & 1, abort_flag, p.err, kErrTimeoutMma))
-          break;
         if (!mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
           break;
-        tc_fence_after();
-        // P occupies 64 packed columns; 16 keys = 8 columns per step.
-        // V block: 16 key rows of 128 bytes per step; D/64 blocks 16 KB apart.
-        const uint64_t vd = desc_add(v_desc, st * C::TILE);
-        const uint32_t pa = tmem + sb * 128;
-        if (j == 0)
-          mma_ts_k<ID_O, 0>(tmem + C::COL_O, pa, vd);
-        else
-          mma_ts_k<ID_O, 1>(tmem + C::COL_O, pa, vd);
+        const bool next = (j + 1 < n_kv);
+        bool k_ready = false;
+#pragma unroll 1
+        for (int x = 0; x < 2; ++x) {
+          if (j >= nx[x]) continue;
+          if (!mbar_wait(bar(C::B_PFULL + x), j & 1, abort_flag, p.err, kErrTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // O_x += P_x V_j: P packed in the first 64 columns of tile x's S.
+          const uint64_t vd = desc_add(v_desc, st * C::TILE);
+          const uint32_t pa = tmem + x * 128;
+          const uint32_t od = tmem + C::COL_O + x * D;
+          if (j == 0)
+            mma_ts_k<ID_O, 0>(od, pa, vd);
+          else
+            mma_ts_k<ID_O, 1>(od, pa, vd);
 #pragma unroll
-        for (int kk = 1; kk < 8; ++kk)
-          mma_ts_k<ID_O, 1>(tmem + C::COL_O, pa + kk * 8, desc_add(vd, kk * 2048));
-        mma_commit(bar(C::B_ODONE));
+          for (int kk = 1; kk < 8; ++kk)
+            mma_ts_k<ID_O, 1>(od, pa + kk * 8, desc_add(vd, kk * 2048));
+          mma_commit(bar(C::B_ODONE + x));
+          if (next && j + 1 < nx[x]) {
+            if (!k_ready) {
+              if (!issue_s_both(j + 1)) {
+                ok = false;
+                break;
+              }
+              k_ready = true;
+            }
+            issue_s(x, j + 1);
+          }
+        }
+        if (!ok) break;
         mma_commit(bar(C::B_VEMPTY + st));
+        if (k_ready) mma_commit(bar(C::B_KEMPTY + (j + 1) % C::NS));
       }
       if (*abort_flag) {
         // Let the MMAs already issued finish before tensor memory is released.
@@ -262,21 +315,27 @@ __global__ void __launch_bounds__(192, 1)
         mbar_wait_timed(bar(C::B_DRAIN), 0);
       }
     }
+  }
   } else {
+    reg_increase<224>();
     // ------------------------------------------------------------ softmax (rows)
-    const int row = threadIdx.x;  // 0..127
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int x = warp >> 2;            // query tile of this warpgroup
+    const int row = threadIdx.x & 127;  // row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int qt = 2 * pair + x;
     const int qi = qt * C::BM + row;
+    const int nt = x == 0 ? nA : nB;
+    const uint32_t col_s = x * 128;
+    const uint32_t col_o = C::COL_O + x * D;
     const float c = p.scale_log2;
     float m_used = -INFINITY;  // reference maximum, log2 domain
     float l = 0.0f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
+    for (int j = 0; j < nt; ++j) {
       // Waits are made warp-uniform: the TMEM loads and stores below are
       // warp-collective, so either every lane goes on or every lane stops.
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + sb), (j >> 1) & 1, abort_flag,
-                                             p.err, kErrTimeoutSoftmax));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + x), j & 1, abort_flag, p.err,
+                                             kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
       float s[128];
@@ -284,7 +343,7 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t r[32];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          tmem_ld32(tmem + lane_off + sb * 128 + q4 * 32, r);
+          tmem_ld32(tmem + lane_off + col_s + q4 * 32, r);
           tmem_wait_ld();
 #pragma unroll
           for (int t = 0; t < 32; ++t) s[q4 * 32 + t] = __uint_as_float(r[t]);
@@ -323,35 +382,36 @@ __global__ void __launch_bounds__(192, 1)
           sum += p0 + p1;
           pk[t] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(tmem + lane_off + sb * 128 + h * 32, pk);
+        tmem_st32(tmem + lane_off + col_s + h * 32, pk);
       }
       l = l * alpha + sum;
       if (j > 0) {
         // O holds P_0..P_{j-1} contributions; it must be final before rescaling.
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE), (j - 1) & 1, abort_flag, p.err,
-                                               kErrTimeoutSoftmax));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
+                                               p.err, kErrTimeoutSoftmax));
         if (!ok) break;
         if (__any_sync(0xffffffffu, upd)) {
           tc_fence_after();
 #pragma unroll
           for (int q4 = 0; q4 < D / 32; ++q4) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_off + C::COL_O + q4 * 32, r);
+            tmem_ld32(tmem + lane_off + col_o + q4 * 32, r);
             tmem_wait_ld();
 #pragma unroll
             for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
-            tmem_st32(tmem + lane_off + C::COL_O + q4 * 32, r);
+            tmem_st32(tmem + lane_off + col_o + q4 * 32, r);
           }
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(bar(C::B_PFULL + sb));
+      mbar_arrive_warp(bar(C::B_PFULL + x));
     }
     // ------------------------------------------------------------ epilogue
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE), (n_kv - 1) & 1, abort_flag,
-                                                   p.err, kErrTimeoutEpilogue));
-    if (ok) {
+    if (ok && nt > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (nt - 1) & 1, abort_flag,
+                                             p.err, kErrTimeoutEpilogue));
+    if (ok && nt > 0) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const bool live = qi < p.N;
@@ -359,7 +419,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int q4 = 0; q4 < D / 32; ++q4) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::COL_O + q4 * 32, r);
+        tmem_ld32(tmem + lane_off + col_o + q4 * 32, r);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
@@ -382,7 +442,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -407,6 +467,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   p.Hq = s.Hq;
   p.G = s.Hq / s.Hkv;
   p.n_qtiles = (s.N + C::BM - 1) / C::BM;
+  p.n_qpairs = (p.n_qtiles + 1) / 2;
   p.n_ktiles = (p.Nk + C::BN - 1) / C::BN;
   p.scale_log2 = s.scale * kLog2e;
   p.err = err;
@@ -422,7 +483,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (hpg > p.n_heads) hpg = p.n_heads;
     p.heads_per_group = static_cast<int>(hpg);
   }
-  const long long grid = static_cast<long long>(s.B) * s.Hq * p.n_qtiles;
+  const long long grid = static_cast<long long>(s.B) * s.Hq * p.n_qpairs;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();

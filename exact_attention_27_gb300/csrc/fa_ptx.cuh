@@ -382,6 +382,21 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ registers
+
+// Per-warpgroup register budget changes (every warp of a warpgroup executes
+// the same one).  The increases must be covered by the block's launch total:
+// sum over warpgroups of 128 x new budget <= threads x registers at launch.
+template <uint32_t N>
+__device__ __forceinline__ void reg_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void reg_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------------------------------ numerics
 
 __device__ __forceinline__ float ex2_approx(float x) {
