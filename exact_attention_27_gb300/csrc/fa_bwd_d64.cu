@@ -60,7 +60,7 @@ struct Cfg64 {
   static constexpr int OFF_DO = OFF_Q + NSQ * TILE;
   static constexpr int OFF_DS = OFF_DO + NSQ * TILE;  // 2 x (128 keys x 128 queries bf16)
   static constexpr int DS_BYTES = 2 * TILE;
-  // L/D ring: NLD slots of one half-step each, L*log2e[64] then D[64]
+  // L/D ring: NLD slots of one half-step each, -L*log2e[64] then -D[64]
   static constexpr int NLD = 6;
   static constexpr int OFF_LD = OFF_DS + 2 * DS_BYTES;
   static constexpr int OFF_BAR = OFF_LD + NLD * 128 * 4;
@@ -344,8 +344,8 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_after();
       const uint32_t sbuf = tmem + lane_off + C::COL_BUF + 128 * a + 32 * wg;
       const float* slot = reinterpret_cast<const float*>(smem + C::OFF_LD) + (h % C::NLD) * 128;
-      const float4* L4 = reinterpret_cast<const float4*>(slot + 32 * wg);
-      const float4* D4 = reinterpret_cast<const float4*>(slot + 64 + 32 * wg);
+      const float4* L4 = reinterpret_cast<const float4*>(slot + 32 * wg);       // -L log2e
+      const float4* D4 = reinterpret_cast<const float4*>(slot + 64 + 32 * wg);  // -D
       uint32_t sv[32], dpv[32];
       tmem_ld32(sbuf, sv);
       tmem_ld32(sbuf + 64, dpv);
@@ -354,24 +354,38 @@ __global__ void __launch_bounds__(448, 1)
       const bool masked = __any_sync(0xffffffffu, (CAUSAL && it == jt) || !key_live);
       tmem_wait_ld();
       uint32_t pk[16], dk16[16];
+      const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
       for (int u4 = 0; u4 < 8; ++u4) {
-        const float4 l4 = L4[u4];
-        const float4 d4 = D4[u4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pv[4], dsv[4];
+        const float4 nl = L4[u4];
+        const float4 nd = D4[u4];
+        float pv[4];
+        // exp2 argument s c - L log2e on pairs
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * u4]), __uint_as_float(sv[4 * u4 + 1])),
+                         c2, f2_pack(nl.x, nl.y)),
+                  pv[0], pv[1]);
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * u4 + 2]), __uint_as_float(sv[4 * u4 + 3])),
+                         c2, f2_pack(nl.z, nl.w)),
+                  pv[2], pv[3]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          pv[e] = ex2_approx(fmaf(__uint_as_float(sv[u4 * 4 + e]), c, -lv[e]));
+        for (int e = 0; e < 4; ++e) pv[e] = ex2_approx(pv[e]);
         if (masked) {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             if (!key_live || (CAUSAL && key > q0 + u4 * 4 + e)) pv[e] = 0.0f;
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          dsv[e] = pv[e] * (__uint_as_float(dpv[u4 * 4 + e]) - dv4[e]);
+        // dS = P o (dP - D) on pairs
+        const uint64_t ds01 = f2_mul(
+            f2_pack(pv[0], pv[1]),
+            f2_add(f2_pack(__uint_as_float(dpv[4 * u4]), __uint_as_float(dpv[4 * u4 + 1])),
+                   f2_pack(nd.x, nd.y)));
+        const uint64_t ds23 = f2_mul(
+            f2_pack(pv[2], pv[3]),
+            f2_add(f2_pack(__uint_as_float(dpv[4 * u4 + 2]), __uint_as_float(dpv[4 * u4 + 3])),
+                   f2_pack(nd.z, nd.w)));
+        float dsv[4];
+        f2_unpack(ds01, dsv[0], dsv[1]);
+        f2_unpack(ds23, dsv[2], dsv[3]);
         pk[2 * u4] = pack_bf16x2(pv[0], pv[1]);
         pk[2 * u4 + 1] = pack_bf16x2(pv[2], pv[3]);
         dk16[2 * u4] = pack_bf16x2(dsv[0], dsv[1]);
@@ -426,17 +440,17 @@ __global__ void __launch_bounds__(448, 1)
       ++wg_phase;
       return __all_sync(0xffffffffu, r);
     };
-    // L*log2e and D of half h into ring slot h % NLD: thread t < 64 loads L
-    // of query t of the half, t >= 64 loads D of query t - 64.  Rows past N
-    // get L = +inf (so P = 0) and D = 0.
+    // -L*log2e and -D of half h into ring slot h % NLD: thread t < 64 loads L
+    // of query t of the half, t >= 64 loads D of query t - 64 (negated, so the
+    // compute warps add them).  Rows past N get -L = -inf (so P = 0), D = 0.
     auto load_ld = [&](int h) -> float {
       if (h >= n_half) return 0.0f;
       int bhq, it;
       step_coords(h >> 1, bhq, it);
       const int qrow = it * C::BQ + (h & 1) * 64 + (t & 63);
-      if (qrow >= p.N) return t < 64 ? INFINITY : 0.0f;
+      if (qrow >= p.N) return t < 64 ? -INFINITY : 0.0f;  // dead rows: P = 0
       const size_t idx = static_cast<size_t>(bhq) * p.N + qrow;
-      return t < 64 ? p.lse[idx] * kLog2e : p.Dvec[idx];
+      return t < 64 ? -p.lse[idx] * kLog2e : -p.Dvec[idx];
     };
     auto store_ld = [&](int h, float val) {
       if (h >= n_half) return;

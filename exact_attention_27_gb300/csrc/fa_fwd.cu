@@ -360,9 +360,17 @@ __global__ void __launch_bounds__(384, 1)
           if (key >= p.Nk || (CAUSAL && key > qpos)) s[t] = -INFINITY;
         }
       }
-      float mx = s[0];
+      // Row max over 8 independent partial maxima (a tree, not a 128-long
+      // chain), two new values per three-input max.
+      float pm[8];
 #pragma unroll
-      for (int t = 1; t < 128; ++t) mx = fmaxf(mx, s[t]);
+      for (int u = 0; u < 8; ++u) pm[u] = fmaxf(s[u], s[u + 8]);
+#pragma unroll
+      for (int t = 16; t < 128; t += 16)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pm[u] = fmax3(pm[u], s[t + u], s[t + u + 8]);
+      const float mx = fmaxf(fmax3(pm[0], pm[1], pm[2]),
+                             fmaxf(fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       const float m_new = fmaxf(m_used, mx * c);
       float alpha = 1.0f;
       const bool upd = m_new > m_used + kRescaleThreshold;
@@ -371,19 +379,29 @@ __global__ void __launch_bounds__(384, 1)
         m_used = m_new;
       }
       const float m_ref = (m_used == -INFINITY) ? 0.0f : m_used;
-      float sum = 0.0f;
+      // exp2(s c - m) with the multiply-add on pairs; 4 independent packed sums.
+      const uint64_t c2 = f2_pack(c, c);
+      const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+      uint64_t ps2[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ps2[u] = 0ull;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
-          const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * t], c, -m_ref));
-          const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * t + 1], c, -m_ref));
-          sum += p0 + p1;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[h * 64 + 2 * t], s[h * 64 + 2 * t + 1]), c2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          ps2[t & 3] = f2_add(ps2[t & 3], f2_pack(p0, p1));
           pk[t] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tmem + lane_off + col_s + h * 32, pk);
       }
+      float sum, sum_hi;
+      f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sum, sum_hi);
+      sum += sum_hi;
       l = l * alpha + sum;
       if (j > 0) {
         // O holds P_0..P_{j-1} contributions; it must be final before rescaling.
