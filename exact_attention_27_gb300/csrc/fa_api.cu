@@ -84,7 +84,7 @@ fa_status validate(int B, int H_q, int H_kv, int N, int d, float scale, int caus
   if (H_q % H_kv != 0) return FA_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARGUMENT;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARGUMENT;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
   const double elems = static_cast<double>(B) * H_q * N * d;
   if (elems >= 1099511627776.0) return FA_ERR_INVALID_ARGUMENT;  // 2^40
   if ((N + 127) / 128 > 65535) return FA_ERR_INVALID_ARGUMENT;   // grid.y limit
@@ -176,7 +176,7 @@ fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, fl
 fa_status fa_backward_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
                                  cudaStream_t stream) {
   if (!o || !dO || !D || rows < 1) return FA_ERR_INVALID_ARGUMENT;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!aligned16(o) || !aligned16(dO) || (reinterpret_cast<uintptr_t>(D) & 3u))
     return FA_ERR_INVALID_ARGUMENT;
   return fa::launch_preprocess(o, dO, D, rows, d, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;

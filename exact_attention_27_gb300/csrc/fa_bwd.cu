@@ -19,28 +19,35 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------ B1
-// D / 8 threads per row, each loading 16 bytes of O and 16 bytes of dO;
-// the partial sums of a row are combined with warp shuffles.
+// TPR threads per row (a power of two, aligned within a warp), each loading
+// VPT 16-byte pieces of O and of dO (pieces part, part + TPR, ...); the
+// partial sums of a row are combined with warp shuffles.
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o,
                                                          const uint4* __restrict__ dO,
                                                          float* __restrict__ out, long long rows) {
-  constexpr int TPR = D / 8;  // threads per row: 8 or 16, aligned within a warp
+  constexpr int PIECES = D / 8;                   // 16-byte pieces per row: 8, 12 or 16
+  constexpr int TPR = (PIECES % 4 == 0 && PIECES % 8 != 0) ? 4 : PIECES;
+  constexpr int VPT = PIECES / TPR;
+  static_assert(TPR * VPT == PIECES && (TPR & (TPR - 1)) == 0, "row split");
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = tid / TPR;
   const int part = static_cast<int>(tid % TPR);
   float acc = 0.0f;
   if (row < rows) {
-    const uint4 a = __ldg(o + row * TPR + part);
-    const uint4 g = __ldg(dO + row * TPR + part);
-    const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t gv[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[t]));
-      const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[t]));
-      acc = fmaf(af.x, gf.x, acc);
-      acc = fmaf(af.y, gf.y, acc);
+    for (int v = 0; v < VPT; ++v) {
+      const uint4 a = __ldg(o + row * PIECES + part + v * TPR);
+      const uint4 g = __ldg(dO + row * PIECES + part + v * TPR);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[t]));
+        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[t]));
+        acc = fmaf(af.x, gf.x, acc);
+        acc = fmaf(af.y, gf.y, acc);
+      }
     }
   }
 #pragma unroll
@@ -82,16 +89,22 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float4* __restri
 // dK is multiplied by scale once at the end; dQ gets its scale in B3.
 //
 // Warp roles (192 threads): warps 0-3 key rows, warp 4 TMA, warp 5 MMA.
-// Tensor memory: dK [0, D), dV [D, 2D), S^T/P^T 128 columns, dP^T 128 columns,
-// dQ 64 columns after dP^T when D = 64, or in dP^T's columns when D = 128.
+// Tensor memory: dK [0, DP), dV [DP, 2DP), S^T/P^T 128 columns, dP^T 128
+// columns, dQ 64 columns after dP^T when D = 64, or in dP^T's columns when
+// DP = 128 (DP = D rounded up to a multiple of 64).
 
+// Head dimension D in {96, 128} (64 has its own kernel).  Tiles are DP = 128
+// columns wide; for D = 96 the copies zero-fill columns 96..127, S^T and dP^T
+// contract over the D real columns, and dV, dK and dQ run at N = DP with
+// zero extra columns that are never stored.
 template <int D>
 struct BwdCfg {
+  static constexpr int DP = (D + 63) / 64 * 64;  // padded head dimension
   static constexpr int BK = 128;                // keys per CTA
   static constexpr int BQ = 128;                // queries per step
-  static constexpr int SUB = D / 64;
+  static constexpr int SUB = DP / 64;
   static constexpr int SUB_BYTES = 128 * 128;
-  static constexpr int TILE = SUB * SUB_BYTES;  // 128 x D bf16
+  static constexpr int TILE = SUB * SUB_BYTES;  // 128 x DP bf16
   static constexpr int NSQ = (D == 64) ? 2 : 1; // Q / dO stages
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
@@ -116,10 +129,10 @@ struct BwdCfg {
   static constexpr int THREADS = 192;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_DK = 0;
-  static constexpr uint32_t COL_DV = D;
-  static constexpr uint32_t COL_S = 2 * D;
-  static constexpr uint32_t COL_DP = 2 * D + 128;
-  static constexpr uint32_t COL_DQ = (D == 64) ? 2 * D + 256 : COL_DP;
+  static constexpr uint32_t COL_DV = DP;
+  static constexpr uint32_t COL_S = 2 * DP;
+  static constexpr uint32_t COL_DP = 2 * DP + 128;
+  static constexpr uint32_t COL_DQ = (D == 64) ? 2 * DP + 256 : COL_DP;
 };
 
 struct BwdParams {
@@ -245,8 +258,8 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t id_kd = idesc_bf16_f32(128, D, false, true);     // dV, dK
-      constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);       // dQ
+      constexpr uint32_t id_kd = idesc_bf16_f32(128, C::DP, false, true);  // dV, dK
+      constexpr uint32_t id_q = idesc_bf16_f32(128, C::DP, true, true);    // dQ
       bool ok = mbar_wait(bar(C::B_KV), 0, abort_flag, p.err, kErrTimeoutMma);
       for (int s = 0; ok && s < n_steps; ++s) {
         const int st = s % C::NSQ;
@@ -262,7 +275,7 @@ __global__ void __launch_bounds__(192, 1)
           mma_ss(tmem + C::COL_S, smem_desc_sw128(sK + off, 16, 1024),
                  smem_desc_sw128(q_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
         }
-        if (D == 128 && s > 0) {
+        if (C::DP == 128 && s > 0) {
           // dQ of the previous step lives in dP^T's columns until drained.
           if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
           tc_fence_after();
@@ -382,26 +395,30 @@ __global__ void __launch_bounds__(192, 1)
                       mbar_wait(bar(C::B_DQFULL), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
+      // D / 32 boxes of 128 rows x 32 fp32, two per pass.
 #pragma unroll
-      for (int pass = 0; pass < (DQ ? D / 64 : 0); ++pass) {
+      for (int pass = 0; pass < (DQ ? (D / 32 + 1) / 2 : 0); ++pass) {
+        constexpr int kBoxes = D / 32;
+        const bool second = 2 * pass + 1 < kBoxes;
         if (t == 0) bulk_wait_group_read0();  // staging free again
         if (!(ok = wg_sync())) break;
         uint32_t a[32], bb[32];
         tmem_ld32(tmem + lane_off + C::COL_DQ + pass * 64, a);
-        tmem_ld32(tmem + lane_off + C::COL_DQ + pass * 64 + 32, bb);
+        if (second) tmem_ld32(tmem + lane_off + C::COL_DQ + pass * 64 + 32, bb);
         tmem_wait_ld();
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           st_shared_v4(sSTG + sw128(t, ch), a[4 * ch], a[4 * ch + 1], a[4 * ch + 2],
                        a[4 * ch + 3]);
-          st_shared_v4(sSTG + C::SUB_BYTES + sw128(t, ch), bb[4 * ch], bb[4 * ch + 1],
-                       bb[4 * ch + 2], bb[4 * ch + 3]);
+          if (second)
+            st_shared_v4(sSTG + C::SUB_BYTES + sw128(t, ch), bb[4 * ch], bb[4 * ch + 1],
+                         bb[4 * ch + 2], bb[4 * ch + 3]);
         }
         fence_proxy_async_smem();
         if (!(ok = wg_sync())) break;
         if (t == 0) {
           tma_reduce_add_3d(&tmdQ, sSTG, pass * 64, q0, bhq);
-          tma_reduce_add_3d(&tmdQ, sSTG + C::SUB_BYTES, pass * 64 + 32, q0, bhq);
+          if (second) tma_reduce_add_3d(&tmdQ, sSTG + C::SUB_BYTES, pass * 64 + 32, q0, bhq);
           bulk_commit_group();
         }
       }
@@ -458,11 +475,14 @@ __global__ void __launch_bounds__(192, 1)
 
 cudaError_t launch_preprocess(const void* o, const void* dO, float* Dout, long long rows, int d,
                               cudaStream_t stream) {
-  const long long threads = rows * (d / 8);
+  const long long threads = rows * (d == 96 ? 4 : d / 8);  // threads per row as in the kernel
   const long long blocks = (threads + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (d == 64)
     preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows);
+  else if (d == 96)
+    preprocess_kernel<96><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows);
   else
     preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
@@ -472,7 +492,7 @@ cudaError_t launch_preprocess(const void* o, const void* dO, float* Dout, long l
 
 cudaError_t launch_dq_finalize(const float* dq_acc, void* dq, long long n, float scale,
                                cudaStream_t stream) {
-  const long long n8 = n / 8;  // n is a multiple of 64
+  const long long n8 = n / 8;  // n = rows x d, a multiple of 32
   const long long blocks = (n8 + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   dq_finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
@@ -511,6 +531,13 @@ cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* Dv,
                             void* dv, const AttnShape& s, uint32_t* err, cudaStream_t stream,
                             bool with_dq) {
   if (s.d == 64) return launch_backward_d64(m, lse, Dv, dk, dv, s, err, stream, with_dq);
+  if (s.d == 96) {
+    if (with_dq)
+      return s.causal ? launch_bwd_t<96, true, true>(m, lse, Dv, dk, dv, s, err, stream)
+                      : launch_bwd_t<96, false, true>(m, lse, Dv, dk, dv, s, err, stream);
+    return s.causal ? launch_bwd_t<96, true, false>(m, lse, Dv, dk, dv, s, err, stream)
+                    : launch_bwd_t<96, false, false>(m, lse, Dv, dk, dv, s, err, stream);
+  }
   if (with_dq)
     return s.causal ? launch_bwd_t<128, true, true>(m, lse, Dv, dk, dv, s, err, stream)
                     : launch_bwd_t<128, false, true>(m, lse, Dv, dk, dv, s, err, stream);

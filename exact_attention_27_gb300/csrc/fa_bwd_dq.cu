@@ -17,7 +17,7 @@
 //
 // Warps: 0-3 one query row per thread, 4 TMA producer, 5 MMA issuer.
 // Tensor memory: S [0,128) (dS as bf16 over its first 64 columns),
-// dP [128,256), dQ [256, 256+D).
+// dP [128,256), dQ [256, 256+DP).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -31,13 +31,17 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Head dimension D in {64, 96, 128}; tiles are DP = D rounded up to a
+// multiple of 64 columns wide (zero-filled past D), S and dP contract over the
+// D real columns and dQ runs at N = DP.
 template <int D>
 struct DqCfg {
+  static constexpr int DP = (D + 63) / 64 * 64;  // padded head dimension
   static constexpr int BM = 128;                 // query rows per CTA
   static constexpr int BN = 128;                 // keys per tile
-  static constexpr int SUB = D / 64;
+  static constexpr int SUB = DP / 64;
   static constexpr int SUB_BYTES = 128 * 128;
-  static constexpr int TILE = SUB * SUB_BYTES;   // 128 x D bf16
+  static constexpr int TILE = SUB * SUB_BYTES;   // 128 x DP bf16
   static constexpr int NS = (D == 64) ? 4 : 2;   // K/V ring stages
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + TILE;
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);  // S, dP
-      constexpr uint32_t ID_Q = idesc_bf16_f32(128, D, false, true);     // dQ (B = K MN-major)
+      constexpr uint32_t ID_Q = idesc_bf16_f32(128, C::DP, false, true);  // dQ (B = K MN-major)
       const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t do_desc = smem_desc_sw128(sdO, 16, 1024);
       const uint64_t k_kmaj = smem_desc_sw128(sK, 16, 1024);
@@ -358,6 +362,9 @@ cudaError_t launch_backward_dq(const BwdMaps& m, const float* lse, const float* 
   if (s.d == 64)
     return s.causal ? launch_dq_t<64, true>(m, lse, Dv, dq, s, err, stream)
                     : launch_dq_t<64, false>(m, lse, Dv, dq, s, err, stream);
+  if (s.d == 96)
+    return s.causal ? launch_dq_t<96, true>(m, lse, Dv, dq, s, err, stream)
+                    : launch_dq_t<96, false>(m, lse, Dv, dq, s, err, stream);
   return s.causal ? launch_dq_t<128, true>(m, lse, Dv, dq, s, err, stream)
                   : launch_dq_t<128, false>(m, lse, Dv, dq, s, err, stream);
 }

@@ -27,7 +27,8 @@
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   columns   0..127  S of tile A    (P as packed bf16 overwrites columns 0..63)
 //   columns 128..255  S of tile B
-//   columns 256..256+2D-1  O accumulators of tiles A and B (fp32)
+//   columns 256..256+2DP-1  O accumulators of tiles A and B (fp32; DP = D
+//              rounded up to a multiple of 64)
 //
 // Online softmax ("L'attention fusionnee", section "Le softmax en ligne"):
 // per key tile m' = max(m, max s), p = exp(s - m'), l = l e^(m - m') + sum p,
@@ -64,11 +65,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
 
+// Head dimension D in {64, 96, 128}.  Tiles are stored DP = D rounded up to
+// a multiple of 64 columns wide (whole 128-byte swizzle atoms); for D = 96
+// the copies fill columns 96..127 with zeros (they lie outside the tensor),
+// Q K^T runs over the D real columns only, and P V runs at N = DP, whose
+// extra output columns stay zero and are never stored.
 template <int D>
 struct FwdCfg {
+  static constexpr int DP = (D + 63) / 64 * 64;  // padded head dimension
   static constexpr int BM = 128;                 // query rows per tile (MMA M)
   static constexpr int BN = 128;                 // keys per tile (MMA N of Q K^T)
-  static constexpr int SUB = D / 64;             // 128-byte column blocks per row
+  static constexpr int SUB = DP / 64;            // 128-byte column blocks per row
   static constexpr int SUB_BYTES = 128 * 128;    // one 128-row x 64-col bf16 block
   static constexpr int TILE = SUB * SUB_BYTES;   // one 128 x D bf16 tile
   static constexpr int NS = (D == 64) ? 4 : 2;   // K/V ring stages
@@ -91,7 +98,7 @@ struct FwdCfg {
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O = 256;         // O of tile x at 256 + x * D
+  static constexpr uint32_t COL_O = 256;         // O of tile x at 256 + x * DP
 };
 
 struct FwdParams {
@@ -232,7 +239,7 @@ __global__ void __launch_bounds__(384, 1)
     // S_B(j+1), so that each tile's softmax overlaps the other tile's MMAs.
     if (elect_one()) {
       constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t ID_O = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t ID_O = idesc_bf16_f32(128, C::DP, false, true);
       const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t k_desc = smem_desc_sw128(sK, 16, 1024);
       const uint64_t v_desc = smem_desc_sw128(sV, C::SUB_BYTES, 1024);
@@ -285,7 +292,7 @@ __global__ void __launch_bounds__(384, 1)
           // O_x += P_x V_j: P packed in the first 64 columns of tile x's S.
           const uint64_t vd = desc_add(v_desc, st * C::TILE);
           const uint32_t pa = tmem + x * 128;
-          const uint32_t od = tmem + C::COL_O + x * D;
+          const uint32_t od = tmem + C::COL_O + x * C::DP;
           if (j == 0)
             mma_ts_k<ID_O, 0>(od, pa, vd);
           else
@@ -326,7 +333,7 @@ __global__ void __launch_bounds__(384, 1)
     const int qi = qt * C::BM + row;
     const int nt = x == 0 ? nA : nB;
     const uint32_t col_s = x * 128;
-    const uint32_t col_o = C::COL_O + x * D;
+    const uint32_t col_o = C::COL_O + x * C::DP;
     const float c = p.scale_log2;
     float m_used = -INFINITY;  // reference maximum, log2 domain
     float l = 0.0f;
@@ -515,6 +522,9 @@ cudaError_t launch_forward(const CUtensorMap& tq, const CUtensorMap& tk, const C
   if (s.d == 64)
     return s.causal ? launch_fwd_t<64, true>(tq, tk, tv, o, lse, s, err, stream)
                     : launch_fwd_t<64, false>(tq, tk, tv, o, lse, s, err, stream);
+  if (s.d == 96)
+    return s.causal ? launch_fwd_t<96, true>(tq, tk, tv, o, lse, s, err, stream)
+                    : launch_fwd_t<96, false>(tq, tk, tv, o, lse, s, err, stream);
   return s.causal ? launch_fwd_t<128, true>(tq, tk, tv, o, lse, s, err, stream)
                   : launch_fwd_t<128, false>(tq, tk, tv, o, lse, s, err, stream);
 }

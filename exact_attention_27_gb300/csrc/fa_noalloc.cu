@@ -59,7 +59,7 @@ extern "C" fa_status fa_backward_noalloc(const void* q, const void* k, const voi
   if (B < 1 || H_q < 1 || H_kv < 1 || N < 1 || H_q % H_kv != 0) return FA_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARGUMENT;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARGUMENT;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
   if ((N + 127) / 128 > 65535) return FA_ERR_INVALID_ARGUMENT;
   const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void* p : p16)

@@ -34,7 +34,7 @@
  *     fa_last_device_error reports a timed-out wait inside a kernel.
  *   - Nothing is printed and nothing aborts.
  *
- * Supported sizes: d in {64, 128}; B, H_q, H_kv, N >= 1; H_q % H_kv == 0;
+ * Supported sizes: d in {64, 96, 128}; B, H_q, H_kv, N >= 1; H_q % H_kv == 0;
  * B * H_q * N * d < 2^40.
  */
 #ifndef FA_H
@@ -49,7 +49,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad size, bad scale */
-  FA_ERR_UNSUPPORTED = 2,      /* d not in {64, 128} */
+  FA_ERR_UNSUPPORTED = 2,      /* d not in {64, 96, 128} */
   FA_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed */
   FA_ERR_DEVICE_TIMEOUT = 4    /* a bounded wait inside a kernel ran out */
 } fa_status;
@@ -183,7 +183,7 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
  *
  *   o, dO  [rows][d] bf16 device pointers, 16-byte aligned, read
  *   D      [rows]    fp32 device pointer, written
- * d in {64, 128}; rows >= 1.  Same return codes as fa_forward.
+ * d in {64, 96, 128}; rows >= 1.  Same return codes as fa_forward.
  */
 fa_status fa_backward_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
                                  cudaStream_t stream);

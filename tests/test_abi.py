@@ -71,7 +71,7 @@ def test_forward_rejects_invalid_arguments(lib, kw):
     assert fwd(lib, **kw) == fa.FA_ERR_INVALID_ARGUMENT
 
 
-@pytest.mark.parametrize("d", [0, 32, 96, 256])
+@pytest.mark.parametrize("d", [0, 32, 80, 160, 256])
 def test_forward_rejects_unsupported_head_dim(lib, d):
     assert fwd(lib, d=d) == fa.FA_ERR_UNSUPPORTED
 

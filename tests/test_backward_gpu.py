@@ -64,12 +64,21 @@ def test_grouped_query_heads(G, d):
     bwd_vs_oracle(inp, True, 1.0 / math.sqrt(d))
 
 
+@pytest.mark.parametrize("N", [1, 70, 129, 600])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_96(N, causal):
+    """d = 96 through the padded 128-column kernels: gradients of the 96 real
+    columns against the oracle; GQA so that dK/dV sum over two heads."""
+    inp = make_inputs(1, 4, 2, N, 96, seed=N + 960, with_grad=True)
+    bwd_vs_oracle(inp, causal, 1.0 / math.sqrt(96))
+
+
 def test_d128_causal_mid_size():
     inp = make_inputs(1, 4, 4, 1024, 128, seed=123, with_grad=True)
     bwd_vs_oracle(inp, True, 1.0 / math.sqrt(128))
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 def test_preprocess_row_dot(d):
     """B1 alone: D = rowsum(dO o O) against the oracle's row_dot."""
     import exact_attention_27_gb300 as fa
@@ -121,6 +130,8 @@ def run_deterministic(inp, causal, scale):
     (2, 8, 2, 300, 64, True),       # grouped-query heads
     (1, 4, 1, 513, 128, False),
     (1, 2, 2, 1, 64, True),
+    (1, 4, 2, 333, 96, True),
+    (1, 2, 1, 200, 96, False),
 ])
 def test_deterministic_backward_against_the_oracle(shape):
     B, Hq, Hkv, N, d, causal = shape

@@ -65,6 +65,27 @@ def test_ragged_lengths(N, d, causal):
     forward_vs_oracle(inp, causal, 1.0 / math.sqrt(d))
 
 
+@pytest.mark.parametrize("N", [1, 70, 128, 257, 1000])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_96(N, causal):
+    """d = 96: tiles padded to 128 columns (zero-filled), 96 stored."""
+    inp = make_inputs(1, 4, 2, N, 96, seed=N + 96)
+    forward_vs_oracle(inp, causal, 1.0 / math.sqrt(96))
+
+
+def test_head_dim_96_query_offset():
+    import exact_attention_27_gb300 as fa
+    inp = make_inputs(2, 4, 1, 200, 96, seed=960, Nk=713)
+    scale = 1.0 / math.sqrt(96)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=scale, q_offset=513)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == 0
+    o_ref, l_ref = oracle.attention_forward(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]),
+                                            scale, True, q_offset=513)
+    check_forward(o, lse, o_ref, l_ref, "d96 offset")
+
+
 @pytest.mark.parametrize("G", [1, 2, 4])
 def test_grouped_query_heads(G):
     inp = make_inputs(2, 8, 8 // G, 384, 128, seed=40 + G)
