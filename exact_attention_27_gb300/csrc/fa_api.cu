@@ -79,12 +79,18 @@ bool make_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long plan
                   CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// K or V of the forward: boxes of one key tile (64 rows when d = 256, else 128).
+bool make_kv_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long planes) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, d, N, planes, 64,
+                  d == 256 ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 fa_status validate(int B, int H_q, int H_kv, int N, int d, float scale, int causal) {
   if (B < 1 || H_q < 1 || H_kv < 1 || N < 1) return FA_ERR_INVALID_ARGUMENT;
   if (H_q % H_kv != 0) return FA_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARGUMENT;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARGUMENT;
-  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   const double elems = static_cast<double>(B) * H_q * N * d;
   if (elems >= 1099511627776.0) return FA_ERR_INVALID_ARGUMENT;  // 2^40
   if ((N + 127) / 128 > 65535) return FA_ERR_INVALID_ARGUMENT;   // grid.y limit
@@ -137,8 +143,8 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
     return FA_ERR_INVALID_ARGUMENT;
   CUtensorMap tq, tk, tv;
   if (!make_map_bf16(&tq, q, d, N, static_cast<long long>(B) * H_q) ||
-      !make_map_bf16(&tk, k, d, N, static_cast<long long>(B) * H_kv) ||
-      !make_map_bf16(&tv, v, d, N, static_cast<long long>(B) * H_kv))
+      !make_kv_map_bf16(&tk, k, d, N, static_cast<long long>(B) * H_kv) ||
+      !make_kv_map_bf16(&tv, v, d, N, static_cast<long long>(B) * H_kv))
     return FA_ERR_CUDA;
   uint32_t* err = error_word();
   if (!err) return FA_ERR_CUDA;
@@ -161,8 +167,8 @@ fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, fl
     return FA_ERR_INVALID_ARGUMENT;
   CUtensorMap tq, tk, tv;
   if (!make_map_bf16(&tq, q, d, N_q, static_cast<long long>(B) * H_q) ||
-      !make_map_bf16(&tk, k, d, N_kv, static_cast<long long>(B) * H_kv) ||
-      !make_map_bf16(&tv, v, d, N_kv, static_cast<long long>(B) * H_kv))
+      !make_kv_map_bf16(&tk, k, d, N_kv, static_cast<long long>(B) * H_kv) ||
+      !make_kv_map_bf16(&tv, v, d, N_kv, static_cast<long long>(B) * H_kv))
     return FA_ERR_CUDA;
   uint32_t* err = error_word();
   if (!err) return FA_ERR_CUDA;
@@ -189,6 +195,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
   const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
   if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;  // forward only
   const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void* p : p16)
     if (!aligned16(p)) return FA_ERR_INVALID_ARGUMENT;
@@ -233,6 +240,7 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
   const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
   if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;  // forward only
   const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void* p : p16)
     if (!aligned16(p)) return FA_ERR_INVALID_ARGUMENT;

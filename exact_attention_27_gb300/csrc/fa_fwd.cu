@@ -519,6 +519,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 cudaError_t launch_forward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            void* o, float* lse, const AttnShape& s, uint32_t* err,
                            cudaStream_t stream) {
+  if (s.d == 256) return launch_forward_d256(tq, tk, tv, o, lse, s, err, stream);
   if (s.d == 64)
     return s.causal ? launch_fwd_t<64, true>(tq, tk, tv, o, lse, s, err, stream)
                     : launch_fwd_t<64, false>(tq, tk, tv, o, lse, s, err, stream);

@@ -19,10 +19,15 @@ struct AttnShape {
 };
 
 // Forward: q/k/v tensor maps (3-D: d, N, B*H; box 64 x 128 x 1; 128-byte
-// swizzle), outputs o (bf16) and lse (fp32).  Returns the launch status.
+// swizzle; for d = 256 the k and v boxes are 64 x 64 x 1), outputs o (bf16)
+// and lse (fp32).  Returns the launch status.
 cudaError_t launch_forward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            void* o, float* lse, const AttnShape& s, uint32_t* err,
                            cudaStream_t stream);
+// The d = 256 forward (fa_fwd_d256.cu), called by launch_forward.
+cudaError_t launch_forward_d256(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, void* o, float* lse, const AttnShape& s,
+                                uint32_t* err, cudaStream_t stream);
 
 // Backward pass kernels (see fa_bwd.cu).
 cudaError_t launch_preprocess(const void* o, const void* dO, float* D, long long rows, int d,

@@ -71,7 +71,7 @@ def test_forward_rejects_invalid_arguments(lib, kw):
     assert fwd(lib, **kw) == fa.FA_ERR_INVALID_ARGUMENT
 
 
-@pytest.mark.parametrize("d", [0, 32, 80, 160, 256])
+@pytest.mark.parametrize("d", [0, 32, 80, 160, 192, 512])
 def test_forward_rejects_unsupported_head_dim(lib, d):
     assert fwd(lib, d=d) == fa.FA_ERR_UNSUPPORTED
 
@@ -82,8 +82,12 @@ def test_backward_rejects_invalid_arguments(lib, kw):
     assert bwd(lib, **kw) == fa.FA_ERR_INVALID_ARGUMENT
 
 
-def test_backward_rejects_unsupported_head_dim(lib):
-    assert bwd(lib, d=80) == fa.FA_ERR_UNSUPPORTED
+@pytest.mark.parametrize("d", [80, 256])
+def test_backward_rejects_unsupported_head_dim(lib, d):
+    """d = 256 has a forward kernel only."""
+    assert bwd(lib, d=d) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_backward_deterministic(P, P, P, P, P, P, P, P, P, 1, 2, 1, 64, d,
+                                         ctypes.c_float(0.125), 1, None) == fa.FA_ERR_UNSUPPORTED
 
 
 def test_preprocess_rejects_invalid_arguments(lib):

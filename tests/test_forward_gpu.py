@@ -86,6 +86,36 @@ def test_head_dim_96_query_offset():
     check_forward(o, lse, o_ref, l_ref, "d96 offset")
 
 
+@pytest.mark.parametrize("N", [1, 63, 64, 65, 200, 1000])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_256(N, causal):
+    """d = 256: one 128-row query tile per CTA, 64-key tiles, S double-buffered."""
+    inp = make_inputs(1, 4, 2, N, 256, seed=N + 256)
+    forward_vs_oracle(inp, causal, 1.0 / math.sqrt(256))
+
+
+def test_head_dim_256_rescaling_and_many_tiles():
+    """Large scores over 48 key tiles exercise the lazy rescale of the 256-column O."""
+    inp = make_inputs(2, 2, 1, 3000, 256, seed=2560)
+    inp["q"] = (inp["q"].float() * 4.0).to(torch.bfloat16)
+    forward_vs_oracle(inp, True, 0.25)
+
+
+@pytest.mark.parametrize("Nq,Nk,off,causal", [(1, 70, 69, True), (100, 513, 413, True),
+                                              (128, 1000, 0, False), (300, 377, 77, True)])
+def test_head_dim_256_query_offset(Nq, Nk, off, causal):
+    import exact_attention_27_gb300 as fa
+    inp = make_inputs(1, 4, 2, Nq, 256, seed=Nq + Nk + 256, Nk=Nk)
+    scale = 1.0 / math.sqrt(256)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o, lse = fa.attention_forward(q, k, v, causal=causal, scale=scale, q_offset=off)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == 0
+    o_ref, l_ref = oracle.attention_forward(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]),
+                                            scale, causal, q_offset=off)
+    check_forward(o, lse, o_ref, l_ref, f"d256 offset {off}")
+
+
 @pytest.mark.parametrize("G", [1, 2, 4])
 def test_grouped_query_heads(G):
     inp = make_inputs(2, 8, 8 // G, 384, 128, seed=40 + G)
