@@ -31,7 +31,8 @@ from workloads import WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "attention TFLOP/s (causal bf16 fwd/bwd) and % of GB300 dense BF16 peak"
 STEP_WORKLOAD = "causal_train_n4096_d64"
-FWD_WORKLOADS = ["causal_n4096_d64", "causal_n8192_d128", "causal_gqa_n16384_d128"]
+FWD_WORKLOADS = ["causal_n4096_d64", "causal_n8192_d128", "causal_gqa_n16384_d128",
+                 "causal_n8192_d96", "causal_n8192_d256", "causal_gqa_n16384_d256"]
 FALLBACK_TFLOPS = 1900.0
 FALLBACK_GBS = 6800.0
 L2_BYTES = 129 * 10**6

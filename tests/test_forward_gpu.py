@@ -142,7 +142,9 @@ def _sampled(w, n_rows, seed):
     return rows
 
 
-@pytest.mark.parametrize("name", ["causal_n8192_d128", "causal_gqa_n16384_d128"])
+@pytest.mark.parametrize("name", ["causal_n8192_d128", "causal_gqa_n16384_d128",
+                                  "causal_n8192_d96", "causal_n8192_d256",
+                                  "causal_gqa_n16384_d256"])
 def test_full_size_sampled_rows(name):
     """Full-size workloads in the benchmark's launch configuration: every head,
     a seeded sample of query rows plus the tile edges, against the oracle."""

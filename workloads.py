@@ -49,7 +49,9 @@ class Workload:
         return f"{kind} {step} B{self.B} {heads} N{self.N} d{self.d} bf16"
 
 
-# The five workloads the attention path is judged on.
+# The workloads of the attention path: five at d = 64 and 128 (the training
+# step and the forward targets), and forward workloads at head dimensions 96
+# and 256.
 WORKLOADS = {
     "single_head_n256": Workload("single_head_n256", 1, 1, 1, 256, 64, False, False),
     "causal_n4096_d64": Workload("causal_n4096_d64", 2, 8, 8, 4096, 64, True, False),
@@ -57,6 +59,10 @@ WORKLOADS = {
     "causal_gqa_n16384_d128": Workload("causal_gqa_n16384_d128", 1, 32, 8, 16384, 128, True,
                                        False),
     "causal_train_n4096_d64": Workload("causal_train_n4096_d64", 2, 8, 8, 4096, 64, True, True),
+    "causal_n8192_d96": Workload("causal_n8192_d96", 4, 16, 16, 8192, 96, True, False),
+    "causal_n8192_d256": Workload("causal_n8192_d256", 2, 16, 16, 8192, 256, True, False),
+    "causal_gqa_n16384_d256": Workload("causal_gqa_n16384_d256", 1, 32, 8, 16384, 256, True,
+                                       False),
 }
 
 
