@@ -222,8 +222,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                      static_cast<long long>(B) * H_q, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
   cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
-  if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, acc_bytes, stream);
-  if (e == cudaSuccess) e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream);
+  if (e == cudaSuccess) e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream, acc);
   const bool timed = g_bwd_before && g_bwd_after;
   if (e == cudaSuccess && timed) e = cudaEventRecord(g_bwd_before, stream);
   if (e == cudaSuccess) e = fa::launch_backward(m, lse, Dbuf, acc, dk, dv, s, err, stream);

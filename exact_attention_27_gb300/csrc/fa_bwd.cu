@@ -21,11 +21,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ------------------------------------------------------------------ B1
 // TPR threads per row (a power of two, aligned within a warp), each loading
 // VPT 16-byte pieces of O and of dO (pieces part, part + TPR, ...); the
-// partial sums of a row are combined with warp shuffles.
+// partial sums of a row are combined with warp shuffles.  When `dq_acc` is not
+// null the same threads also zero the row of the fp32 dQ accumulator (the
+// 32 bytes that match each 16-byte piece), which saves a separate memset.
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o,
                                                          const uint4* __restrict__ dO,
-                                                         float* __restrict__ out, long long rows) {
+                                                         float* __restrict__ out, long long rows,
+                                                         float4* __restrict__ dq_acc) {
   constexpr int PIECES = D / 8;                   // 16-byte pieces per row: 8, 12 or 16
   constexpr int TPR = (PIECES % 4 == 0 && PIECES % 8 != 0) ? 4 : PIECES;
   constexpr int VPT = PIECES / TPR;
@@ -37,8 +40,13 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
   if (row < rows) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-      const uint4 a = __ldg(o + row * PIECES + part + v * TPR);
-      const uint4 g = __ldg(dO + row * PIECES + part + v * TPR);
+      const long long piece = row * PIECES + part + v * TPR;
+      const uint4 a = __ldg(o + piece);
+      const uint4 g = __ldg(dO + piece);
+      if (dq_acc) {
+        dq_acc[2 * piece] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dq_acc[2 * piece + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       const uint32_t av[4] = {a.x, a.y, a.z, a.w};
       const uint32_t gv[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
@@ -474,19 +482,20 @@ __global__ void __launch_bounds__(192, 1)
 }  // namespace
 
 cudaError_t launch_preprocess(const void* o, const void* dO, float* Dout, long long rows, int d,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, float* zero_acc) {
+  float4* acc = reinterpret_cast<float4*>(zero_acc);
   const long long threads = rows * (d == 96 ? 4 : d / 8);  // threads per row as in the kernel
   const long long blocks = (threads + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (d == 64)
     preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows);
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows, acc);
   else if (d == 96)
     preprocess_kernel<96><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows);
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows, acc);
   else
     preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows);
+        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows, acc);
   return cudaGetLastError();
 }
 

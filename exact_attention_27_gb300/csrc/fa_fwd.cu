@@ -345,16 +345,17 @@ __global__ void __launch_bounds__(384, 1)
                                              kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
+      // The row's 128 scores: four loads in flight, one wait.
       float s[128];
       {
-        uint32_t r[32];
+        uint32_t r[128];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          tmem_ld32(tmem + lane_off + col_s + q4 * 32, r);
-          tmem_wait_ld();
+        for (int q4 = 0; q4 < 4; ++q4)
+          tmem_ld32(tmem + lane_off + col_s + q4 * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&r[q4 * 32]));
+        tmem_wait_ld();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) s[q4 * 32 + t] = __uint_as_float(r[t]);
-        }
+        for (int t = 0; t < 128; ++t) s[t] = __uint_as_float(r[t]);
       }
       const int kbase = j * C::BN;
       const int qpos = p.q_offset + qi;  // absolute position of this row

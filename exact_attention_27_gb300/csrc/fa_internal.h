@@ -30,8 +30,10 @@ cudaError_t launch_forward_d256(const CUtensorMap& tq, const CUtensorMap& tk,
                                 uint32_t* err, cudaStream_t stream);
 
 // Backward pass kernels (see fa_bwd.cu).
+// D = rowsum(dO o O) per row; if zero_acc is not null, also zeroes the fp32
+// dQ accumulator [rows][d] (16-byte aligned).
 cudaError_t launch_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
-                              cudaStream_t stream);
+                              cudaStream_t stream, float* zero_acc = nullptr);
 
 struct BwdMaps {
   CUtensorMap q, k, v, dO;  // bf16, box 64 x 128 x 1, 128-byte swizzle

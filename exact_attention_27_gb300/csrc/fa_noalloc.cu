@@ -72,7 +72,6 @@ extern "C" fa_status fa_backward_noalloc(const void* q, const void* k, const voi
   if (need > static_cast<double>(FA_NOALLOC_SCRATCH_BYTES)) return FA_ERR_INVALID_ARGUMENT;
   const long long rows = static_cast<long long>(B) * H_q * N;
   const size_t acc_off = (static_cast<size_t>(rows) * 4 + 1023) & ~static_cast<size_t>(1023);
-  const size_t acc_bytes = static_cast<size_t>(rows) * d * 4;
 
   void* base = scratch_address();
   uint32_t* err = fa::device_error_word();
@@ -88,9 +87,8 @@ extern "C" fa_status fa_backward_noalloc(const void* q, const void* k, const voi
                   fa::encode_map_f32_acc(&m.dq_acc, acc, d, N, static_cast<long long>(B) * H_q);
   if (!ok) return FA_ERR_CUDA;
   fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
-  // The accumulator keeps the previous call's sums: clear it first.
-  cudaError_t e = cudaMemsetAsync(acc, 0, acc_bytes, stream);
-  if (e == cudaSuccess) e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream);
+  // The accumulator keeps the previous call's sums: the preprocess clears it.
+  cudaError_t e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream, acc);
   if (e == cudaSuccess) e = fa::launch_backward(m, lse, Dbuf, acc, dk, dv, s, err, stream);
   if (e == cudaSuccess) e = fa::launch_dq_finalize(acc, dq, rows * d, scale, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
