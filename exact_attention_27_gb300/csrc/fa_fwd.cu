@@ -92,13 +92,19 @@ struct FwdCfg {
   static constexpr int B_SFULL = B_VEMPTY + NS;  // [2] per query tile
   static constexpr int B_PFULL = B_SFULL + 2;    // [2] per query tile (4 warp arrivals)
   static constexpr int B_ODONE = B_PFULL + 2;    // [2] per query tile
-  static constexpr int B_DRAIN = B_ODONE + 2;    // abort path: MMAs in flight
+  static constexpr int B_SFREE = B_ODONE + 2;    // [2] S of a tile loaded by its softmax (SEP_P)
+  static constexpr int B_DRAIN = B_SFREE + 2;    // abort path: MMAs in flight
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort word
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = 256;         // O of tile x at 256 + x * DP
+  // At DP = 64 the 128 columns after the two O accumulators hold P (bf16) of
+  // each tile, so S_x(j+1) can be computed into S_x while the softmax still
+  // works on P_x(j).  At DP = 128 P overwrites S.
+  static constexpr bool SEP_P = (DP == 64);
+  static constexpr uint32_t COL_P = 384;         // SEP_P: P of tile x at 384 + 64 x
 };
 
 struct FwdParams {
@@ -168,6 +174,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::B_SFULL + x), 1);
       mbar_init(bar(C::B_PFULL + x), 4);  // one arrival per softmax warp of the tile
       mbar_init(bar(C::B_ODONE + x), 1);
+      mbar_init(bar(C::B_SFREE + x), 4);  // one arrival per softmax warp of the tile
     }
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -275,7 +282,55 @@ __global__ void __launch_bounds__(384, 1)
           mma_commit(bar(C::B_KEMPTY + 0));
         }
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
+      if constexpr (C::SEP_P) {
+        // Per key tile j: S_A(j+1), S_B(j+1), each once its tile's softmax
+        // has loaded S(j) (they then run under that softmax), then
+        // O_A += P_A V_j and O_B += P_B V_j as the P tiles arrive.
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int st = j % C::NS;
+          if (j + 1 < n_kv) {
+            if (!issue_s_both(j + 1)) break;
+#pragma unroll 1
+            for (int x = 0; x < 2; ++x) {
+              if (j + 1 >= nx[x]) continue;
+              if (!mbar_wait(bar(C::B_SFREE + x), j & 1, abort_flag, p.err, kErrTimeoutMma)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(x, j + 1);
+            }
+            if (!ok) break;
+            mma_commit(bar(C::B_KEMPTY + (j + 1) % C::NS));
+          }
+          if (!mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err,
+                         kErrTimeoutMma))
+            break;
+#pragma unroll 1
+          for (int x = 0; x < 2; ++x) {
+            if (j >= nx[x]) continue;
+            if (!mbar_wait(bar(C::B_PFULL + x), j & 1, abort_flag, p.err, kErrTimeoutMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t vd = desc_add(v_desc, st * C::TILE);
+            const uint32_t pa = tmem + C::COL_P + x * 64;
+            const uint32_t od = tmem + C::COL_O + x * C::DP;
+            if (j == 0)
+              mma_ts_k<ID_O, 0>(od, pa, vd);
+            else
+              mma_ts_k<ID_O, 1>(od, pa, vd);
+#pragma unroll
+            for (int kk = 1; kk < 8; ++kk)
+              mma_ts_k<ID_O, 1>(od, pa + kk * 8, desc_add(vd, kk * 2048));
+            mma_commit(bar(C::B_ODONE + x));
+          }
+          if (!ok) break;
+          mma_commit(bar(C::B_VEMPTY + st));
+        }
+      }
+      for (int j = 0; !C::SEP_P && ok && j < n_kv; ++j) {
         const int st = j % C::NS;
         if (!mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
           break;
@@ -334,6 +389,7 @@ __global__ void __launch_bounds__(384, 1)
     const int nt = x == 0 ? nA : nB;
     const uint32_t col_s = x * 128;
     const uint32_t col_o = C::COL_O + x * C::DP;
+    const uint32_t col_p = C::SEP_P ? C::COL_P + x * 64 : col_s;  // P as packed bf16
     const float c = p.scale_log2;
     float m_used = -INFINITY;  // reference maximum, log2 domain
     float l = 0.0f;
@@ -356,6 +412,19 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int t = 0; t < 128; ++t) s[t] = __uint_as_float(r[t]);
+      }
+      if constexpr (C::SEP_P) {
+        // S_x is in registers: the next S may be computed into its columns.
+        tc_fence_before();
+        mbar_arrive_warp(bar(C::B_SFREE + x));
+        // P_x(j) goes where O += P_x(j-1) V reads from: wait for that product
+        // (it also has to be done before O is rescaled below).
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
+                                                 p.err, kErrTimeoutSoftmax));
+          if (!ok) break;
+          tc_fence_after();
+        }
       }
       const int kbase = j * C::BN;
       const int qpos = p.q_offset + qi;  // absolute position of this row
@@ -405,17 +474,20 @@ __global__ void __launch_bounds__(384, 1)
           ps2[t & 3] = f2_add(ps2[t & 3], f2_pack(p0, p1));
           pk[t] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(tmem + lane_off + col_s + h * 32, pk);
+        tmem_st32(tmem + lane_off + col_p + h * 32, pk);
       }
       float sum, sum_hi;
       f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sum, sum_hi);
       sum += sum_hi;
       l = l * alpha + sum;
       if (j > 0) {
-        // O holds P_0..P_{j-1} contributions; it must be final before rescaling.
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
-                                               p.err, kErrTimeoutSoftmax));
-        if (!ok) break;
+        // O holds P_0..P_{j-1} contributions; it must be final before rescaling
+        // (with SEP_P this was waited for before P was stored).
+        if (!C::SEP_P) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
+                                                 p.err, kErrTimeoutSoftmax));
+          if (!ok) break;
+        }
         if (__any_sync(0xffffffffu, upd)) {
           tc_fence_after();
 #pragma unroll
