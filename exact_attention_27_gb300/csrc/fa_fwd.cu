@@ -417,14 +417,6 @@ __global__ void __launch_bounds__(384, 1)
         // S_x is in registers: the next S may be computed into its columns.
         tc_fence_before();
         mbar_arrive_warp(bar(C::B_SFREE + x));
-        // P_x(j) goes where O += P_x(j-1) V reads from: wait for that product
-        // (it also has to be done before O is rescaled below).
-        if (j > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
-                                                 p.err, kErrTimeoutSoftmax));
-          if (!ok) break;
-          tc_fence_after();
-        }
       }
       const int kbase = j * C::BN;
       const int qpos = p.q_offset + qi;  // absolute position of this row
@@ -462,20 +454,31 @@ __global__ void __launch_bounds__(384, 1)
       uint64_t ps2[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) ps2[u] = 0ull;
+      // The whole row of P is formed in registers before it is stored, so the
+      // wait below for the previous O += P V (whose P columns these are when
+      // SEP_P) comes after the exponentials rather than before them.
+      uint32_t pk[64];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[h * 64 + 2 * t], s[h * 64 + 2 * t + 1]), c2, nm2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          ps2[t & 3] = f2_add(ps2[t & 3], f2_pack(p0, p1));
-          pk[t] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tmem + lane_off + col_p + h * 32, pk);
+      for (int t = 0; t < 64; ++t) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(s[2 * t], s[2 * t + 1]), c2, nm2), x0, x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        ps2[t & 3] = f2_add(ps2[t & 3], f2_pack(p0, p1));
+        pk[t] = pack_bf16x2(p0, p1);
       }
+      if constexpr (C::SEP_P) {
+        // P_x(j) goes where O += P_x(j-1) V reads from: wait for that product
+        // (it also has to be done before O is rescaled below).
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
+                                                 p.err, kErrTimeoutSoftmax));
+          if (!ok) break;
+          tc_fence_after();
+        }
+      }
+      tmem_st32(tmem + lane_off + col_p, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tmem + lane_off + col_p + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       float sum, sum_hi;
       f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sum, sum_hi);
       sum += sum_hi;
