@@ -50,13 +50,19 @@ def peaks():
         return FALLBACK_TFLOPS, FALLBACK_GBS, "fallback"
 
 
+# The source file of each kernel named in profiles/traffic.txt.
+KERNEL_SOURCES = {"fa_bwd64_kernel": "fa_bwd_d64.cu", "fa_fwd_kernel": "fa_fwd.cu",
+                  "fa_fwd256_kernel": "fa_fwd_d256.cu", "fa_bwd_kernel": "fa_bwd.cu",
+                  "fa_bwd_dq_kernel": "fa_bwd_dq.cu"}
+
+
 def kernel_traffic(kernel):
     """Bytes per launch from the committed ncu summary, if the kernel's source
     is unchanged since the capture (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    src_hash = source_hash()
+    src_hash = source_hash(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel:
@@ -65,12 +71,13 @@ def kernel_traffic(kernel):
     return None
 
 
-def source_hash():
+def source_hash(kernel):
+    """Hash of the kernel's own source file and the headers it includes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_27_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    base = kernel.split("<")[0]
+    for f in (KERNEL_SOURCES[base], "fa_ptx.cuh", "fa_internal.h"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
