@@ -256,6 +256,7 @@ def run_ours(args, rank, world):
         result["clocks"] = clocks.summary()
         if not args.only_step:
             result["fwd_workloads"] = forward_workloads(fa, torch, tflops_peak, peak_src)
+            result["fwd_workloads"].append(forward_fp8_workload(fa, torch, tflops_peak, peak_src))
             result["e2e"] = end_to_end(fa, torch, w, min(K, 50))
             if world == 1:
                 result["cpu_baseline"] = cpu_baseline(w)
@@ -322,6 +323,39 @@ def forward_workloads(fa, torch, tflops_peak, peak_src):
                     "input_sets": R})
         del sets, inp
         torch.cuda.empty_cache()
+    return out
+
+
+def forward_fp8_workload(fa, torch, tflops_peak, peak_src):
+    """The FP8 forward (e4m3 Q, K, V^T; unit descales) on the shape of the
+    causal d = 128 workload, against twice the measured bf16 peak (the
+    nominal FP8 : bf16 dense tensor ratio)."""
+    w = WORKLOADS["causal_n8192_d128"]
+    inp = make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, seed=7)
+    q = inp["q"].to(torch.float8_e4m3fn).cuda()
+    k = inp["k"].to(torch.float8_e4m3fn).cuda()
+    vt = inp["v"].to(torch.float8_e4m3fn).transpose(-1, -2).contiguous().cuda()
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        fa.fa_forward_fp8(q, k, vt, o, lse, w.scale, w.causal)
+    reps = 20
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s_ev.record()
+    for _ in range(reps):
+        fa.fa_forward_fp8(q, k, vt, o, lse, w.scale, w.causal)
+    e_ev.record()
+    torch.cuda.synchronize()
+    ms = s_ev.elapsed_time(e_ev) / reps
+    tf = w.fwd_flops() / (ms * 1e-3) / 1e12
+    peak = 2.0 * tflops_peak
+    out = {"workload": w.describe().replace("bf16", "e4m3 (O bf16)"), "dtype": "e4m3",
+           "ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / peak, 4),
+           "peak": f"2 x {peak_src} bf16 burst (nominal fp8/bf16 ratio)",
+           "input_sets": 1}
+    del q, k, vt, o, lse
+    torch.cuda.empty_cache()
     return out
 
 

@@ -18,7 +18,7 @@ import math
 from ._lib import FaError, library, status_string  # noqa: F401
 
 __all__ = [
-    "FaError", "fa_forward", "fa_forward_ex", "fa_backward", "fa_backward_deterministic", "fa_backward_preprocess", "fa_status_string",
+    "FaError", "fa_forward", "fa_forward_ex", "fa_forward_fp8", "fa_backward", "fa_backward_deterministic", "fa_backward_preprocess", "fa_status_string",
     "fa_last_device_error", "fa_selftest_wait_timeout", "fa_set_backward_events", "attention_forward", "attention_backward",
     "library",
 ]
@@ -99,6 +99,27 @@ def fa_forward_ex(q, k, v, o, lse, scale, causal, q_offset=0, stream=None):
                                    lse.data_ptr(), B, Hq, Hkv, Nq, Nk, d, ctypes.c_float(scale),
                                    int(bool(causal)), int(q_offset), _stream(stream)),
            "fa_forward_ex")
+
+
+def fa_forward_fp8(q, k, v_t, o, lse, scale, causal, q_descale=1.0, k_descale=1.0,
+                   v_descale=1.0, stream=None):
+    """fa_forward_fp8 of include/fa.h: q [B,H_q,N,d], k [B,H_kv,N,d] and the
+    transposed v_t [B,H_kv,d,N] as float8_e4m3fn tensors (values times their
+    descales); writes o (bf16) and lse (fp32)."""
+    import torch
+    B, Hq, Hkv, N, d = _shapes(q, k)
+    for name, t, shp in (("q", q, None), ("k", k, None), ("v_t", v_t, (B, Hkv, d, N))):
+        if t.dtype != torch.float8_e4m3fn or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float8_e4m3fn CUDA tensor")
+        if shp is not None and tuple(t.shape) != tuple(shp):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shp)}")
+    _bf16_cuda("o", o, q.shape)
+    _f32_cuda("lse", lse, (B, Hq, N))
+    _check(library().fa_forward_fp8(q.data_ptr(), k.data_ptr(), v_t.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), B, Hq, Hkv, N, d, ctypes.c_float(scale),
+                                    ctypes.c_float(q_descale), ctypes.c_float(k_descale),
+                                    ctypes.c_float(v_descale), int(bool(causal)),
+                                    _stream(stream)), "fa_forward_fp8")
 
 
 def fa_backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, stream=None):

@@ -179,6 +179,37 @@ fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, fl
                                                                                : FA_ERR_CUDA;
 }
 
+fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o, float* lse,
+                         int B, int H_q, int H_kv, int N, int d, float scale, float q_descale,
+                         float k_descale, float v_descale, int causal, cudaStream_t stream) {
+  if (!q || !k || !v_t || !o || !lse) return FA_ERR_INVALID_ARGUMENT;
+  const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  for (float f : {q_descale, k_descale, v_descale})
+    if (!std::isfinite(f) || !(f > 0.0f)) return FA_ERR_INVALID_ARGUMENT;
+  const float s_eff = scale * q_descale * k_descale;
+  if (!std::isfinite(s_eff) || !(s_eff > 0.0f)) return FA_ERR_INVALID_ARGUMENT;
+  if (N % 16 != 0) return FA_ERR_INVALID_ARGUMENT;  // V^T rows of N bytes: 16-byte strides
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v_t) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_INVALID_ARGUMENT;
+  CUtensorMap tq, tk, tvt;
+  if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q, d, N, static_cast<long long>(B) * H_q,
+                128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, k, d, N, static_cast<long long>(B) * H_kv,
+                128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&tvt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, v_t, N, d,
+                static_cast<long long>(B) * H_kv, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return FA_ERR_CUDA;
+  uint32_t* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  fa::AttnShape s{B, H_q, H_kv, N, d, s_eff, causal};
+  return fa::launch_forward_fp8(tq, tk, tvt, o, lse, s, v_descale, err, stream) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
 fa_status fa_backward_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
                                  cudaStream_t stream) {
   if (!o || !dO || !D || rows < 1) return FA_ERR_INVALID_ARGUMENT;

@@ -70,15 +70,20 @@ constexpr float kRescaleThreshold = 8.0f;
 // the copies fill columns 96..127 with zeros (they lie outside the tensor),
 // Q K^T runs over the D real columns only, and P V runs at N = DP, whose
 // extra output columns stay zero and are never stored.
-template <int D>
+//
+// FP8 = true: Q, K and V^T are e4m3 (one byte per element, D = 128: one
+// 128-byte row per tile row, so SUB = 1), the products run as kind::f8f6f4,
+// P is rounded to e4m3 (4 per TMEM column) and V comes transposed ([d][N]),
+// so that both operands of O += P V are K-major.
+template <int D, bool FP8 = false>
 struct FwdCfg {
   static constexpr int DP = (D + 63) / 64 * 64;  // padded head dimension
   static constexpr int BM = 128;                 // query rows per tile (MMA M)
   static constexpr int BN = 128;                 // keys per tile (MMA N of Q K^T)
-  static constexpr int SUB = DP / 64;            // 128-byte column blocks per row
-  static constexpr int SUB_BYTES = 128 * 128;    // one 128-row x 64-col bf16 block
-  static constexpr int TILE = SUB * SUB_BYTES;   // one 128 x D bf16 tile
-  static constexpr int NS = (D == 64) ? 4 : 2;   // K/V ring stages
+  static constexpr int SUB = FP8 ? 1 : DP / 64;  // 128-byte column blocks per row
+  static constexpr int SUB_BYTES = 128 * 128;    // one 128-row x 128-byte block
+  static constexpr int TILE = SUB * SUB_BYTES;   // one 128 x D tile
+  static constexpr int NS = (D == 64 || FP8) ? 4 : 2;  // K/V ring stages
   static constexpr int OFF_Q = 0;                // two query tiles
   static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
@@ -103,7 +108,7 @@ struct FwdCfg {
   // At DP = 64 the 128 columns after the two O accumulators hold P (bf16) of
   // each tile, so S_x(j+1) can be computed into S_x while the softmax still
   // works on P_x(j).  At DP = 128 P overwrites S.
-  static constexpr bool SEP_P = (DP == 64);
+  static constexpr bool SEP_P = (DP == 64) && !FP8;
   static constexpr uint32_t COL_P = 384;         // SEP_P: P of tile x at 384 + 64 x
 };
 
@@ -120,15 +125,16 @@ struct FwdParams {
   int n_ktiles;
   int n_heads;          // B * Hq
   int heads_per_group;  // launch-order grouping, a multiple of G
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // scale * log2(e) (times the Q and K descales for FP8)
+  float o_scale;     // factor on O in the epilogue (the V descale for FP8, else 1)
   uint32_t* err;
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool FP8 = false>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -225,10 +231,16 @@ __global__ void __launch_bounds__(384, 1)
             !mbar_wait(bar(C::B_VEMPTY + st), ph, abort_flag, p.err, kErrTimeoutLoad))
           break;
         mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE);
+        if constexpr (FP8) {
+          // V^T: 128 rows of d, each 128 keys (bytes) long.
+          tma_load_3d_hint(sV + st * C::TILE, &tmV, bar(C::B_VFULL + st), j * C::BN, 0, kvz,
+                           keep);
+        } else {
 #pragma unroll
-        for (int s = 0; s < C::SUB; ++s)
-          tma_load_3d_hint(sV + st * C::TILE + s * C::SUB_BYTES, &tmV, bar(C::B_VFULL + st),
-                           64 * s, j * C::BN, kvz, keep);
+          for (int s = 0; s < C::SUB; ++s)
+            tma_load_3d_hint(sV + st * C::TILE + s * C::SUB_BYTES, &tmV, bar(C::B_VFULL + st),
+                             64 * s, j * C::BN, kvz, keep);
+        }
         issued = j + 1;
       }
       if (*abort_flag) {
@@ -245,11 +257,14 @@ __global__ void __launch_bounds__(384, 1)
     // Order: S_A(0) S_B(0), then per key tile j: PV_A(j) S_A(j+1) PV_B(j)
     // S_B(j+1), so that each tile's softmax overlaps the other tile's MMAs.
     if (elect_one()) {
-      constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t ID_O = idesc_bf16_f32(128, C::DP, false, true);
+      constexpr uint32_t ID_S =
+          FP8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t ID_O =
+          FP8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, C::DP, false, true);
       const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t k_desc = smem_desc_sw128(sK, 16, 1024);
-      const uint64_t v_desc = smem_desc_sw128(sV, C::SUB_BYTES, 1024);
+      // bf16: V is [keys][d], read MN-major; FP8: V^T is [d][keys], read K-major.
+      const uint64_t v_desc = smem_desc_sw128(sV, FP8 ? 16 : C::SUB_BYTES, 1024);
       const int nx[2] = {nA, nB};
       bool ok = mbar_wait(bar(C::B_QFULL), 0, abort_flag, p.err, kErrTimeoutMma);
       // S_x(j) = Q_x K_j^T into tile x's S columns.
@@ -257,11 +272,19 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t d_tmem = tmem + x * 128;
         const uint64_t qd = desc_add(q_desc, x * C::TILE);
         const uint64_t kd = desc_add(k_desc, (j % C::NS) * C::TILE);
-        mma_ss_k<ID_S, 0>(d_tmem, qd, kd);
+        if constexpr (FP8) {
+          // 32 e4m3 elements (32 bytes) of d per step.
+          mma_ss_f8_k<ID_S, 0>(d_tmem, qd, kd);
 #pragma unroll
-        for (int kk = 1; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          mma_ss_k<ID_S, 1>(d_tmem, desc_add(qd, off), desc_add(kd, off));
+          for (int kk = 1; kk < D / 32; ++kk)
+            mma_ss_f8_k<ID_S, 1>(d_tmem, desc_add(qd, kk * 32), desc_add(kd, kk * 32));
+        } else {
+          mma_ss_k<ID_S, 0>(d_tmem, qd, kd);
+#pragma unroll
+          for (int kk = 1; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+            mma_ss_k<ID_S, 1>(d_tmem, desc_add(qd, off), desc_add(kd, off));
+          }
         }
         mma_commit(bar(C::B_SFULL + x));
       };
@@ -344,17 +367,28 @@ __global__ void __launch_bounds__(384, 1)
             break;
           }
           tc_fence_after();
-          // O_x += P_x V_j: P packed in the first 64 columns of tile x's S.
+          // O_x += P_x V_j: P packed over the first columns of tile x's S
+          // (bf16: 16 keys = 8 columns per step; e4m3: 32 keys = 8 columns).
           const uint64_t vd = desc_add(v_desc, st * C::TILE);
           const uint32_t pa = tmem + x * 128;
           const uint32_t od = tmem + C::COL_O + x * C::DP;
-          if (j == 0)
-            mma_ts_k<ID_O, 0>(od, pa, vd);
-          else
-            mma_ts_k<ID_O, 1>(od, pa, vd);
+          if constexpr (FP8) {
+            if (j == 0)
+              mma_ts_f8_k<ID_O, 0>(od, pa, vd);
+            else
+              mma_ts_f8_k<ID_O, 1>(od, pa, vd);
 #pragma unroll
-          for (int kk = 1; kk < 8; ++kk)
-            mma_ts_k<ID_O, 1>(od, pa + kk * 8, desc_add(vd, kk * 2048));
+            for (int kk = 1; kk < 4; ++kk)
+              mma_ts_f8_k<ID_O, 1>(od, pa + kk * 8, desc_add(vd, kk * 32));
+          } else {
+            if (j == 0)
+              mma_ts_k<ID_O, 0>(od, pa, vd);
+            else
+              mma_ts_k<ID_O, 1>(od, pa, vd);
+#pragma unroll
+            for (int kk = 1; kk < 8; ++kk)
+              mma_ts_k<ID_O, 1>(od, pa + kk * 8, desc_add(vd, kk * 2048));
+          }
           mma_commit(bar(C::B_ODONE + x));
           if (next && j + 1 < nx[x]) {
             if (!k_ready) {
@@ -457,28 +491,46 @@ __global__ void __launch_bounds__(384, 1)
       // The whole row of P is formed in registers before it is stored, so the
       // wait below for the previous O += P V (whose P columns these are when
       // SEP_P) comes after the exponentials rather than before them.
-      uint32_t pk[64];
+      if constexpr (FP8) {
+        // P rounded to e4m3, four keys per TMEM column (the lowest key in the
+        // lowest byte); the running sum uses the fp32 values.
+        uint32_t pk8[32];
 #pragma unroll
-      for (int t = 0; t < 64; ++t) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(s[2 * t], s[2 * t + 1]), c2, nm2), x0, x1);
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
-        ps2[t & 3] = f2_add(ps2[t & 3], f2_pack(p0, p1));
-        pk[t] = pack_bf16x2(p0, p1);
-      }
-      if constexpr (C::SEP_P) {
-        // P_x(j) goes where O += P_x(j-1) V reads from: wait for that product
-        // (it also has to be done before O is rescaled below).
-        if (j > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
-                                                 p.err, kErrTimeoutSoftmax));
-          if (!ok) break;
-          tc_fence_after();
+        for (int t = 0; t < 32; ++t) {
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(s[4 * t], s[4 * t + 1]), c2, nm2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(s[4 * t + 2], s[4 * t + 3]), c2, nm2), x2, x3);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          ps2[(2 * t) & 3] = f2_add(ps2[(2 * t) & 3], f2_pack(p0, p1));
+          ps2[(2 * t + 1) & 3] = f2_add(ps2[(2 * t + 1) & 3], f2_pack(p2, p3));
+          pk8[t] = pack_e4m3x4(p0, p1, p2, p3);
         }
+        tmem_st32(tmem + lane_off + col_p, pk8);
+      } else {
+        uint32_t pk[64];
+  #pragma unroll
+        for (int t = 0; t < 64; ++t) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[2 * t], s[2 * t + 1]), c2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          ps2[t & 3] = f2_add(ps2[t & 3], f2_pack(p0, p1));
+          pk[t] = pack_bf16x2(p0, p1);
+        }
+        if constexpr (C::SEP_P) {
+          // P_x(j) goes where O += P_x(j-1) V reads from: wait for that product
+          // (it also has to be done before O is rescaled below).
+          if (j > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
+                                                   p.err, kErrTimeoutSoftmax));
+            if (!ok) break;
+            tc_fence_after();
+          }
+        }
+        tmem_st32(tmem + lane_off + col_p, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tmem + lane_off + col_p + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       }
-      tmem_st32(tmem + lane_off + col_p, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tmem + lane_off + col_p + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       float sum, sum_hi;
       f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sum, sum_hi);
       sum += sum_hi;
@@ -514,7 +566,7 @@ __global__ void __launch_bounds__(384, 1)
                                              p.err, kErrTimeoutEpilogue));
     if (ok && nt > 0) {
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      const float inv_l = p.o_scale / l;
       const bool live = qi < p.N;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + (live ? qi : 0)) * D;
 #pragma unroll
@@ -550,12 +602,12 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool FP8 = false>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          void* o, float* lse, const AttnShape& s, uint32_t* err,
-                         cudaStream_t stream) {
-  using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL>;
+                         cudaStream_t stream, float o_scale = 1.0f) {
+  using C = FwdCfg<D, FP8>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, FP8>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -571,12 +623,13 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   p.n_qpairs = (p.n_qtiles + 1) / 2;
   p.n_ktiles = (p.Nk + C::BN - 1) / C::BN;
   p.scale_log2 = s.scale * kLog2e;
+  p.o_scale = o_scale;
   p.err = err;
   p.n_heads = s.B * s.Hq;
   {
     // Group query heads so that the K/V they read (shared within a GQA
     // group) stays within about 48 MiB of the 129 MB L2.
-    const double kv_bytes = 2.0 * p.Nk * D * 2.0;  // one K/V head
+    const double kv_bytes = 2.0 * p.Nk * D * (FP8 ? 1.0 : 2.0);  // one K/V head
     const double budget = 48.0 * 1024 * 1024;
     long long kv_heads = static_cast<long long>(budget / kv_bytes);
     if (kv_heads < 1) kv_heads = 1;
@@ -604,6 +657,13 @@ cudaError_t launch_forward(const CUtensorMap& tq, const CUtensorMap& tk, const C
                     : launch_fwd_t<96, false>(tq, tk, tv, o, lse, s, err, stream);
   return s.causal ? launch_fwd_t<128, true>(tq, tk, tv, o, lse, s, err, stream)
                   : launch_fwd_t<128, false>(tq, tk, tv, o, lse, s, err, stream);
+}
+
+cudaError_t launch_forward_fp8(const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tvt, void* o, float* lse, const AttnShape& s,
+                               float v_descale, uint32_t* err, cudaStream_t stream) {
+  return s.causal ? launch_fwd_t<128, true, true>(tq, tk, tvt, o, lse, s, err, stream, v_descale)
+                  : launch_fwd_t<128, false, true>(tq, tk, tvt, o, lse, s, err, stream, v_descale);
 }
 
 }  // namespace fa

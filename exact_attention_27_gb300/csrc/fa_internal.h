@@ -24,6 +24,12 @@ struct AttnShape {
 cudaError_t launch_forward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            void* o, float* lse, const AttnShape& s, uint32_t* err,
                            cudaStream_t stream);
+// FP8 forward, d = 128: q, k maps over e4m3 [.., N, 128] with 128 x 128-byte
+// boxes, tvt over V^T e4m3 [.., 128, N_kv] with 128 x 128-byte boxes; s.scale
+// already includes the Q and K descales, O is multiplied by v_descale.
+cudaError_t launch_forward_fp8(const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tvt, void* o, float* lse, const AttnShape& s,
+                               float v_descale, uint32_t* err, cudaStream_t stream);
 // The d = 256 forward (fa_fwd_d256.cu), called by launch_forward.
 cudaError_t launch_forward_d256(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, void* o, float* lse, const AttnShape& s,

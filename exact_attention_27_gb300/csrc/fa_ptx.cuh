@@ -267,6 +267,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0)
+// and an fp32 accumulator, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | ((static_cast<uint32_t>(N) >> 3) << 17) |
+         ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -307,6 +314,27 @@ __device__ __forceinline__ void mma_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint6
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "n"(IDESC), "n"(ACC)
+      : "memory");
+}
+
+// The same products for e4m3 operands (32 elements of K per instruction).
+template <uint32_t IDESC, uint32_t ACC>
+__device__ __forceinline__ void mma_ss_f8_k(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "n"(IDESC), "n"(ACC)
+      : "memory");
+}
+
+template <uint32_t IDESC, uint32_t ACC>
+__device__ __forceinline__ void mma_ts_f8_k(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "n"(IDESC), "n"(ACC)
       : "memory");
 }
@@ -441,6 +469,19 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// Four fp32 -> four e4m3 bytes (round to nearest even, saturating to the
+// largest finite value); `a` lands in the lowest byte, `d` in the highest.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` lands in the low half.

@@ -34,7 +34,8 @@
  *     fa_last_device_error reports a timed-out wait inside a kernel.
  *   - Nothing is printed and nothing aborts.
  *
- * Supported sizes: d in {64, 96, 128}; B, H_q, H_kv, N >= 1; H_q % H_kv == 0;
+ * Supported sizes: d in {64, 96, 128} (and 256 for fa_forward and fa_forward_ex);
+ * B, H_q, H_kv, N >= 1; H_q % H_kv == 0;
  * B * H_q * N * d < 2^40.
  */
 #ifndef FA_H
@@ -49,7 +50,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad size, bad scale */
-  FA_ERR_UNSUPPORTED = 2,      /* d not in {64, 96, 128} */
+  FA_ERR_UNSUPPORTED = 2,      /* head dimension d not supported by the call */
   FA_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed */
   FA_ERR_DEVICE_TIMEOUT = 4    /* a bounded wait inside a kernel ran out */
 } fa_status;
@@ -93,6 +94,29 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
 fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H_q, int H_kv, int N_q, int N_kv, int d, float scale, int causal,
                         int q_offset, cudaStream_t stream);
+
+/*
+ * FP8 forward.  "FlashAttention: l'attenzione che non spreca memoria", section
+ * on what comes next: the tensor cores gain narrower formats down to FP8
+ * (8 bits), which halve again the bytes to move.  The same computation as
+ * fa_forward with Q, K and V stored as e4m3 (OCP FP8, 4 exponent and 3
+ * mantissa bits) times one fp32 factor per tensor, the products Q K^T and
+ * P V on the FP8 tensor cores with fp32 accumulation, the softmax in fp32,
+ * and P rounded to e4m3 (round to nearest even) for P V.
+ *
+ *   q    [B][H_q][N][d]   e4m3, read; its values are q * q_descale
+ *   k    [B][H_kv][N][d]  e4m3, read; values k * k_descale
+ *   v_t  [B][H_kv][d][N]  e4m3, read: V transposed (N contiguous), values
+ *                         v_t * v_descale (every operand is then K-major)
+ *   o    [B][H_q][N][d]   bf16, written;  lse [B][H_q][N] fp32, written
+ *
+ * d = 128 only (else FA_ERR_UNSUPPORTED); N a multiple of 16 (the rows of
+ * v_t are N bytes long and must start 16 bytes apart); q_descale, k_descale,
+ * v_descale finite and > 0.  Otherwise as fa_forward.
+ */
+fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o, float* lse,
+                         int B, int H_q, int H_kv, int N, int d, float scale, float q_descale,
+                         float k_descale, float v_descale, int causal, cudaStream_t stream);
 
 /*
  * Backward pass.  Source: "L'attention fusionnee", section "La passe

@@ -132,3 +132,21 @@ def test_forward_ex_rejects_invalid_arguments(lib, kw):
 
 def test_forward_ex_rejects_unsupported_head_dim(lib):
     assert fwd_ex(lib, d=32) == fa.FA_ERR_UNSUPPORTED
+
+
+def fwd_fp8(lib, d=128, N=64, q=P, vt=P, qd=1.0, kd=1.0, vd=1.0, causal=1):
+    return lib.fa_forward_fp8(q, P, vt, P, P, 1, 2, 1, N, d, ctypes.c_float(0.125),
+                              ctypes.c_float(qd), ctypes.c_float(kd), ctypes.c_float(vd), causal,
+                              None)
+
+
+@pytest.mark.parametrize("kw", [dict(N=72), dict(N=1), dict(qd=0.0), dict(kd=-1.0),
+                                dict(vd=float("nan")), dict(vd=float("inf")), dict(q=None),
+                                dict(vt=Q), dict(causal=2), dict(qd=1e30, kd=1e30)])
+def test_forward_fp8_rejects_invalid_arguments(lib, kw):
+    assert fwd_fp8(lib, **kw) == fa.FA_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("d", [64, 96, 256])
+def test_forward_fp8_rejects_unsupported_head_dim(lib, d):
+    assert fwd_fp8(lib, d=d) == fa.FA_ERR_UNSUPPORTED
