@@ -52,7 +52,7 @@ def peaks():
 
 # The source file of each kernel named in profiles/traffic.txt.
 KERNEL_SOURCES = {"fa_bwd64_kernel": "fa_bwd_d64.cu", "fa_fwd_kernel": "fa_fwd.cu",
-                  "fa_fwd256_kernel": "fa_fwd_d256.cu", "fa_bwd_kernel": "fa_bwd.cu",
+                  "fa_fwd1_kernel": "fa_fwd_tile1.cu", "fa_bwd_kernel": "fa_bwd.cu",
                   "fa_bwd_dq_kernel": "fa_bwd_dq.cu"}
 
 

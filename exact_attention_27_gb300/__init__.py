@@ -18,7 +18,8 @@ import math
 from ._lib import FaError, library, status_string  # noqa: F401
 
 __all__ = [
-    "FaError", "fa_forward", "fa_forward_ex", "fa_forward_fp8", "fa_backward", "fa_backward_deterministic", "fa_backward_preprocess", "fa_status_string",
+    "FaError", "fa_forward", "fa_forward_ex", "fa_forward_fp8", "fa_set_forward_tile_rows",
+    "fa_backward", "fa_backward_deterministic", "fa_backward_preprocess", "fa_status_string",
     "fa_last_device_error", "fa_selftest_wait_timeout", "fa_set_backward_events", "attention_forward", "attention_backward",
     "library",
 ]
@@ -120,6 +121,11 @@ def fa_forward_fp8(q, k, v_t, o, lse, scale, causal, q_descale=1.0, k_descale=1.
                                     ctypes.c_float(q_descale), ctypes.c_float(k_descale),
                                     ctypes.c_float(v_descale), int(bool(causal)),
                                     _stream(stream)), "fa_forward_fp8")
+
+
+def fa_set_forward_tile_rows(rows):
+    """fa_set_forward_tile_rows of include/fa.h: 0 (per shape), 128 or 256."""
+    _check(library().fa_set_forward_tile_rows(int(rows)), "fa_set_forward_tile_rows")
 
 
 def fa_backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, stream=None):

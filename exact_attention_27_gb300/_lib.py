@@ -40,6 +40,8 @@ def _declare(lib):
     lib.fa_forward_ex.restype = i
     lib.fa_forward_ex.argtypes = [p, p, p, p, p, i, i, i, i, i, i, f, i, i, p]
     lib.fa_forward_fp8.restype = i
+    lib.fa_set_forward_tile_rows.restype = i
+    lib.fa_set_forward_tile_rows.argtypes = [i]
     lib.fa_forward_fp8.argtypes = [p, p, p, p, p, i, i, i, i, i, f, f, f, f, i, p]
     lib.fa_backward.restype = i
     lib.fa_backward.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, p]

@@ -324,6 +324,12 @@ fa_status fa_last_device_error(cudaStream_t stream) {
   return FA_ERR_DEVICE_TIMEOUT;
 }
 
+fa_status fa_set_forward_tile_rows(int rows) {
+  if (rows != 0 && rows != 128 && rows != 256) return FA_ERR_INVALID_ARGUMENT;
+  fa::set_forward_rows_per_cta(rows);
+  return FA_OK;
+}
+
 void fa_set_backward_events(cudaEvent_t before, cudaEvent_t after) {
   g_bwd_before = before;
   g_bwd_after = after;

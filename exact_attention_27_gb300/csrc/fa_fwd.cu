@@ -55,6 +55,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -643,12 +645,45 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   return cudaGetLastError();
 }
 
+// Query rows per CTA: 128 (fa_fwd_tile1.cu) or 256 (two tiles here); 0 lets
+// use_one_tile_per_cta decide per shape.
+std::atomic<int> g_rows_per_cta{0};
+
+// The per-shape choice between one and two query tiles per CTA.  Two tiles
+// per CTA share each K/V tile between two softmax warpgroups; one tile per
+// CTA makes twice as many CTAs, which wins while the two-tile grid would
+// leave SMs idle or load them unevenly.  Measured on GB300 (152 SMs; d = 64
+// and 128, causal and not, B*H from 2 to 64, N from 1024 to 8192): one tile
+// per CTA is 1.1-1.9x faster while the two-tile grid has fewer CTAs than
+// SMs under the causal mask (fewer than half as many without it), and
+// 0.75-0.95x as fast beyond.
+bool use_one_tile_per_cta(const AttnShape& s) {
+  const int forced = g_rows_per_cta.load(std::memory_order_relaxed);
+  if (forced == 128) return true;
+  if (forced == 256) return false;
+  static int sms = [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 148;
+    return n;
+  }();
+  const long long qtiles = (static_cast<long long>(s.N) + 127) / 128;
+  const long long pair_ctas = static_cast<long long>(s.B) * s.Hq * ((qtiles + 1) / 2);
+  return pair_ctas * (s.causal ? 1 : 2) < sms;
+}
+
 }  // namespace
+
+void set_forward_rows_per_cta(int rows) { g_rows_per_cta.store(rows); }
+int forward_rows_per_cta() { return g_rows_per_cta.load(); }
 
 cudaError_t launch_forward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            void* o, float* lse, const AttnShape& s, uint32_t* err,
                            cudaStream_t stream) {
-  if (s.d == 256) return launch_forward_d256(tq, tk, tv, o, lse, s, err, stream);
+  if (s.d == 256) return launch_forward_tile1(tq, tk, tv, o, lse, s, err, stream);
+  if ((s.d == 64 || s.d == 128) && use_one_tile_per_cta(s))
+    return launch_forward_tile1(tq, tk, tv, o, lse, s, err, stream);
   if (s.d == 64)
     return s.causal ? launch_fwd_t<64, true>(tq, tk, tv, o, lse, s, err, stream)
                     : launch_fwd_t<64, false>(tq, tk, tv, o, lse, s, err, stream);

@@ -1,11 +1,14 @@
-// Forward pass of exact attention for head dimension 256 on sm_103a.
+// Forward pass of exact attention on sm_103a with one query tile per CTA.
 //
 // Same mathematics as fa_fwd.cu ("FlashAttention: l'attenzione che non spreca
 // memoria", section "L'idea: lavorare a tessere, mai scrivere la matrice";
 // online softmax as in "L'attention fusionnee", section "Le softmax en
-// ligne"), with tiles sized for d = 256: a 128 x 256 bf16 query tile is
-// 64 KB and its fp32 O accumulator takes 256 of the 512 tensor-memory
-// columns, so one CTA holds one query tile, and keys come in tiles of 64.
+// ligne") with a query block of B_r = 128 rows per CTA instead of fa_fwd.cu's
+// two tiles (B_r = 256).  It is the only forward for d = 256 (a 128 x 256
+// bf16 query tile is 64 KB and its fp32 O takes 256 of the 512 TMEM columns,
+// so keys come in tiles of 64 there), and the alternative tile size for
+// d = 64 and 128 (keys in tiles of 128): twice as many CTAs, which covers the
+// SMs better when there are few query tiles.
 //
 // Pipeline: the S tile of key tile j is computed into tensor-memory buffer
 // j mod 3, so the tensor core computes S_{j+1} and S_{j+2} (and O += P_j V_j)
@@ -24,9 +27,9 @@
 //              O += P_j V_j, S_{j+2} = Q K_{j+2}^T into buffer (j+2) mod 3.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
-//   columns 64b..64b+63  S buffer b = 0, 1, 2 (P as packed bf16 over its
-//                        first 32 columns)
-//   columns 256..511     O accumulator (fp32)
+//   columns BN*b .. BN*b + BN - 1   S buffer b = 0, 1, 2 (P as packed bf16
+//                                   over its first BN/2 columns)
+//   columns 512 - D .. 511          O accumulator (fp32)
 //
 // Every mbarrier wait is bounded (about a second); on expiry the kernel sets
 // an error bit, every role skips its remaining work and the CTA exits.
@@ -45,16 +48,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
 
-struct Cfg256 {
-  static constexpr int D = 256;
+template <int D_>
+struct Cfg1 {
+  static constexpr int D = D_;                   // 64, 128 or 256
   static constexpr int BM = 128;                 // query rows per tile (MMA M)
-  static constexpr int BN = 64;                  // keys per tile (MMA N of Q K^T)
+  static constexpr int BN = D == 256 ? 64 : 128; // keys per tile (MMA N of Q K^T)
   static constexpr int SUB = D / 64;             // 128-byte column blocks per row
   static constexpr int Q_BLOCK = BM * 128;       // one 128-row x 64-col block
-  static constexpr int KV_BLOCK = BN * 128;      // one 64-row x 64-col block
-  static constexpr int Q_TILE = SUB * Q_BLOCK;   // 64 KB
-  static constexpr int KV_TILE = SUB * KV_BLOCK; // 32 KB
-  static constexpr int NS = 2;                   // K/V ring stages
+  static constexpr int KV_BLOCK = BN * 128;      // one BN-row x 64-col block
+  static constexpr int Q_TILE = SUB * Q_BLOCK;
+  static constexpr int KV_TILE = SUB * KV_BLOCK;
+  static constexpr int NS = D == 64 ? 4 : 2;     // K/V ring stages
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_TILE;
   static constexpr int OFF_V = OFF_K + NS * KV_TILE;
@@ -76,10 +80,11 @@ struct Cfg256 {
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 192;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O = 256;
+  static constexpr uint32_t COL_O = 512 - D;   // above the NB S buffers
+  static_assert(NB * BN <= 512 - D, "tensor memory");
 };
 
-struct Fwd256Params {
+struct Fwd1Params {
   __nv_bfloat16* o;
   float* lse;
   int N;         // query rows
@@ -95,12 +100,12 @@ struct Fwd256Params {
   uint32_t* err;
 };
 
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(192, 1)
-    fa_fwd256_kernel(const __grid_constant__ CUtensorMap tmQ,
-                     const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const Fwd256Params p) {
-  using C = Cfg256;
+    fa_fwd1_kernel(const __grid_constant__ CUtensorMap tmQ,
+                   const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Fwd1Params p) {
+  using C = Cfg1<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t ID_O = idesc_bf16_f32(128, C::D, false, true);
       const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t k_desc = smem_desc_sw128(sK, 16, 1024);
-      const uint64_t v_desc = smem_desc_sw128(sV, C::KV_BLOCK, 1024);  // MN-major, N = 256
+      const uint64_t v_desc = smem_desc_sw128(sV, C::KV_BLOCK, 1024);  // MN-major, N = D
       bool ok = mbar_wait(bar(C::B_QFULL), 0, abort_flag, p.err, kErrTimeoutMma);
       // S_j = Q K_j^T into buffer j % NB (16 steps of 16 columns of d); K_j is
       // released when the product is done.
@@ -339,7 +344,11 @@ __global__ void __launch_bounds__(192, 1)
           ps2[t & 3] = f2_add(ps2[t & 3], f2_pack(p0, p1));
           pk[t] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(tmem + lane_off + col_s, pk);  // P over the S columns just read
+        // P over the S columns just read.
+#pragma unroll
+        for (int q4 = 0; q4 < C::BN / 64; ++q4)
+          tmem_st32(tmem + lane_off + col_s + q4 * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&pk[q4 * 32]));
       }
       float sum, sum_hi;
       f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sum, sum_hi);
@@ -410,15 +419,15 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,
                      float* lse, const AttnShape& s, uint32_t* err, cudaStream_t stream) {
-  using C = Cfg256;
-  auto kern = fa_fwd256_kernel<CAUSAL>;
+  using C = Cfg1<D>;
+  auto kern = fa_fwd1_kernel<D, CAUSAL>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  Fwd256Params p;
+  Fwd1Params p;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.N = s.N;
@@ -449,13 +458,21 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 
 }  // namespace
 
-// K and V maps must have boxes of 64 rows (the key tile) x 64 columns; the
-// query map boxes of 128 rows x 64 columns.
-cudaError_t launch_forward_d256(const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, void* o, float* lse, const AttnShape& s,
-                                uint32_t* err, cudaStream_t stream) {
-  return s.causal ? launch_t<true>(tq, tk, tv, o, lse, s, err, stream)
-                  : launch_t<false>(tq, tk, tv, o, lse, s, err, stream);
+// d in {64, 128, 256}.  K and V maps have boxes of one key tile (64 rows
+// for d = 256, else 128) x 64 columns; the query map boxes of 128 x 64.
+cudaError_t launch_forward_tile1(const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, void* o, float* lse, const AttnShape& s,
+                                 uint32_t* err, cudaStream_t stream) {
+  if (s.d == 256)
+    return s.causal ? launch_t<256, true>(tq, tk, tv, o, lse, s, err, stream)
+                    : launch_t<256, false>(tq, tk, tv, o, lse, s, err, stream);
+  if (s.d == 128)
+    return s.causal ? launch_t<128, true>(tq, tk, tv, o, lse, s, err, stream)
+                    : launch_t<128, false>(tq, tk, tv, o, lse, s, err, stream);
+  if (s.d == 64)
+    return s.causal ? launch_t<64, true>(tq, tk, tv, o, lse, s, err, stream)
+                    : launch_t<64, false>(tq, tk, tv, o, lse, s, err, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

@@ -30,10 +30,14 @@ cudaError_t launch_forward(const CUtensorMap& tq, const CUtensorMap& tk, const C
 cudaError_t launch_forward_fp8(const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tvt, void* o, float* lse, const AttnShape& s,
                                float v_descale, uint32_t* err, cudaStream_t stream);
-// The d = 256 forward (fa_fwd_d256.cu), called by launch_forward.
-cudaError_t launch_forward_d256(const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, void* o, float* lse, const AttnShape& s,
-                                uint32_t* err, cudaStream_t stream);
+// The forward with one query tile per CTA (fa_fwd_tile1.cu), d in {64, 128,
+// 256}; launch_forward chooses it (always for d = 256).
+cudaError_t launch_forward_tile1(const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, void* o, float* lse, const AttnShape& s,
+                                 uint32_t* err, cudaStream_t stream);
+// Query rows per CTA for the forward: 0 = chosen per shape, 128 or 256.
+void set_forward_rows_per_cta(int rows);
+int forward_rows_per_cta();
 
 // Backward pass kernels (see fa_bwd.cu).
 // D = rowsum(dO o O) per row; if zero_acc is not null, also zeroes the fp32

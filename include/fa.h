@@ -119,6 +119,22 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o,
                          float k_descale, float v_descale, int causal, cudaStream_t stream);
 
 /*
+ * Query rows per CTA of the bf16 forward (fa_forward, fa_forward_ex) at
+ * d = 64 and 128 — the B_r of the tiling in "FlashAttention: l'attenzione che
+ * non spreca memoria", section "L'idea: lavorare a tessere", chosen per
+ * problem size as the autotuning row of "Flash Attention ... NVIDIA CUDA
+ * Tile", section "Resumen: La pila de optimización", does per sequence length:
+ *   0    chosen per shape (the default): 256 unless that grid would leave
+ *        the GPU's SMs short of work, then 128;
+ *   128  one 128-row query tile per CTA;
+ *   256  two 128-row query tiles per CTA sharing each K/V tile.
+ * Both give the same results up to rounding order.  d = 96 always uses 256,
+ * d = 256 always 128.  Process-wide; returns FA_ERR_INVALID_ARGUMENT for any
+ * other value.
+ */
+fa_status fa_set_forward_tile_rows(int rows);
+
+/*
  * Backward pass.  Source: "L'attention fusionnee", section "La passe
  * arriere : recalculer plutot que garder": P is rebuilt tile by tile from the saved L as p = exp(s - L);
  *   dV = P^T dO;  dS = P o (dO V^T - D) with D = rowsum(dO o O);

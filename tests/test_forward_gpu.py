@@ -217,3 +217,42 @@ def test_forward_ex_with_equal_lengths_is_forward():
     o2, l2 = fa.attention_forward(q, k, v, causal=True, q_offset=0)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.fixture
+def tile_rows():
+    import exact_attention_27_gb300 as fa
+    yield fa.fa_set_forward_tile_rows
+    fa.fa_set_forward_tile_rows(0)
+
+
+@pytest.mark.parametrize("rows", [128, 256])
+@pytest.mark.parametrize("N,d,causal,Hq,Hkv", [
+    (1, 64, True, 2, 1), (129, 64, False, 2, 2), (700, 64, True, 4, 2), (1000, 128, True, 2, 1),
+    (257, 128, False, 4, 4), (2048, 64, True, 2, 2),
+])
+def test_both_tile_sizes_against_the_oracle(tile_rows, rows, N, d, causal, Hq, Hkv):
+    """One (128 rows) or two (256) query tiles per CTA, forced, at d = 64 and 128."""
+    tile_rows(rows)
+    inp = make_inputs(1, Hq, Hkv, N, d, seed=N + d + rows)
+    forward_vs_oracle(inp, causal, 1.0 / math.sqrt(d))
+
+
+@pytest.mark.parametrize("rows", [128, 256])
+def test_both_tile_sizes_with_query_offset(tile_rows, rows):
+    import exact_attention_27_gb300 as fa
+    tile_rows(rows)
+    inp = make_inputs(1, 4, 2, 300, 128, seed=31, Nk=941)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=0.1, q_offset=641)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attention_forward(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]),
+                                            0.1, True, q_offset=641)
+    check_forward(o, lse, o_ref, l_ref, f"rows {rows}")
+
+
+def test_tile_rows_rejects_other_values():
+    import exact_attention_27_gb300 as fa
+    with pytest.raises(fa.FaError):
+        fa.fa_set_forward_tile_rows(64)
+    fa.fa_set_forward_tile_rows(0)
