@@ -33,6 +33,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
   constexpr int TPR = (PIECES % 4 == 0 && PIECES % 8 != 0) ? 4 : PIECES;
   constexpr int VPT = PIECES / TPR;
   static_assert(TPR * VPT == PIECES && (TPR & (TPR - 1)) == 0, "row split");
+  // The backward's main kernel, launched as a dependent, may start its own
+  // set-up now; it waits for this grid before reading D or the accumulator.
+  grid_launch_dependents();
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = tid / TPR;
   const int part = static_cast<int>(tid % TPR);
@@ -68,8 +71,9 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float4* __restri
                                                           uint4* __restrict__ dq, long long n8,
                                                           float scale) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  grid_dependency_wait();  // the accumulator is complete once the main kernel is
   if (i >= n8) return;
-  const float4 a = __ldg(acc + 2 * i);
+  const float4 a = __ldcg(acc + 2 * i);
   const float4 b = __ldg(acc + 2 * i + 1);
   dq[i] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
                      pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
@@ -330,6 +334,9 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ key rows
+    // L and D are read, and dQ reduced into the accumulator, only once the
+    // row-dot pass (the grid before this one) has completed.
+    grid_dependency_wait();
     const int t = threadIdx.x;  // key row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const int key = jt * C::BK + t;
@@ -436,6 +443,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (t == 0) bulk_wait_group0();
     __syncwarp();  // lane 0 waited alone; the TMEM loads below are warp-collective
+    grid_launch_dependents();  // the dQ finalisation may be scheduled
     // ---- epilogue: dK (times scale) and dV, one key row per thread
     if (ok) {
       tc_fence_after();
@@ -504,9 +512,9 @@ cudaError_t launch_dq_finalize(const float* dq_acc, void* dq, long long n, float
   const long long n8 = n / 8;  // n = rows x d, a multiple of 32
   const long long blocks = (n8 + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  dq_finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(dq_acc), static_cast<uint4*>(dq), n8, scale);
-  return cudaGetLastError();
+  return launch_dependent(dq_finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                          stream, reinterpret_cast<const float4*>(dq_acc),
+                          static_cast<uint4*>(dq), n8, scale);
 }
 
 template <int D, bool CAUSAL, bool DQ>
@@ -532,8 +540,8 @@ cudaError_t launch_bwd_t(const BwdMaps& m, const float* lse, const float* Dv, vo
   p.err = err;
   const int n_ktiles = (s.N + C::BK - 1) / C::BK;
   dim3 grid(static_cast<unsigned>(s.B * s.Hkv), static_cast<unsigned>(n_ktiles));
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dO, m.dq_acc, p);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, m.q, m.k, m.v,
+                          m.dO, m.dq_acc, p);
 }
 
 cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* Dv, float*, void* dk,

@@ -410,6 +410,10 @@ __global__ void __launch_bounds__(448, 1)
   } else if (wg == 2) {
     // ------------------------------------------------------------ K/V -> TMEM, dQ drain, epilogue
     const int t = threadIdx.x & 127;
+    // This warpgroup alone reads what the row-dot pass (the grid before this
+    // one) writes: D, and the zeroed dQ accumulator the reduces add into.
+    // The other roles start on K, V, Q and dO right away.
+    grid_dependency_wait();
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t wg_phase = 0;
     bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KV), 0, abort_flag, p.err,
@@ -506,6 +510,7 @@ __global__ void __launch_bounds__(448, 1)
     }
     if (t == 0) bulk_wait_group0();
     __syncwarp();  // lane 0 waited alone; the TMEM loads below are warp-collective
+    grid_launch_dependents();  // the dQ finalisation may be scheduled
     // ---- epilogue, once every MMA has completed
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_FINAL), 0, abort_flag, p.err,
                                                    kErrTimeoutEpilogue));
@@ -577,9 +582,8 @@ cudaError_t launch_t(const BwdMaps& m, const float* lse, const float* Dv, void* 
   const long long n_ktiles = (s.N + C::BK - 1) / C::BK;
   const long long grid = n_ktiles * s.B * s.Hkv;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dO,
-                                                                         m.dq_acc, p);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS),
+                          C::SMEM_BYTES, stream, m.q, m.k, m.v, m.dO, m.dq_acc, p);
 }
 
 }  // namespace

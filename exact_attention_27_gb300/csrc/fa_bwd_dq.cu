@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ query rows
+    grid_dependency_wait();  // D comes from the row-dot pass, before the dK/dV grid
     const int row = threadIdx.x;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const int qi = qt * C::BM + row;
@@ -350,9 +351,8 @@ cudaError_t launch_dq_t(const BwdMaps& m, const float* lse, const float* Dv, voi
   p.err = err;
   const long long grid = static_cast<long long>(p.n_heads) * p.n_qtiles;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(m.q, m.k, m.v, m.dO,
-                                                                         p);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS),
+                          C::SMEM_BYTES, stream, m.q, m.k, m.v, m.dO, p);
 }
 
 }  // namespace

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 namespace fa {
 
@@ -35,6 +36,25 @@ cudaError_t launch_forward_fp8(const CUtensorMap& tq, const CUtensorMap& tk,
 cudaError_t launch_forward_tile1(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, void* o, float* lse, const AttnShape& s,
                                  uint32_t* err, cudaStream_t stream);
+// Launches kern<<<grid, block, smem, stream>>>(args...) as a programmatic
+// dependent of the previous grid in the stream (the kernel must call
+// grid_dependency_wait before reading what that grid writes).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Query rows per CTA for the forward: 0 = chosen per shape, 128 or 256.
 void set_forward_rows_per_cta(int rows);
 int forward_rows_per_cta();

@@ -133,6 +133,23 @@ __device__ __forceinline__ bool mbar_wait_timed(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// ------------------------------------------------------------------ dependent launches
+
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialisation may start while the previous grid in the stream still runs;
+// grid_dependency_wait() blocks the calling thread until that grid has
+// completed and its memory operations are visible.  Only threads that read
+// what the previous grid writes need to call it.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid in the stream (if launched as a dependent) be scheduled
+// once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
