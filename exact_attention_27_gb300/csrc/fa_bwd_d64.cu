@@ -410,10 +410,6 @@ __global__ void __launch_bounds__(448, 1)
   } else if (wg == 2) {
     // ------------------------------------------------------------ K/V -> TMEM, dQ drain, epilogue
     const int t = threadIdx.x & 127;
-    // This warpgroup alone reads what the row-dot pass (the grid before this
-    // one) writes: D, and the zeroed dQ accumulator the reduces add into.
-    // The other roles start on K, V, Q and dO right away.
-    grid_dependency_wait();
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t wg_phase = 0;
     bool ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_KV), 0, abort_flag, p.err,
@@ -461,6 +457,11 @@ __global__ void __launch_bounds__(448, 1)
       reinterpret_cast<float*>(smem + C::OFF_LD)[(h % C::NLD) * 128 + t] = val;
       mbar_arrive_warp(bar(C::B_LDFULL + h % C::NLD));
     };
+    // This warpgroup alone reads what the row-dot pass (the grid before this
+    // one) writes: D, and the zeroed dQ accumulator the reduces add into.
+    // Everything before this point (and the other roles' K, V, Q and dO
+    // loads and first products) may run while that grid drains.
+    grid_dependency_wait();
     // Halves of tiles 0..2 first; then, once the compute warps have read the
     // slots of tile s, the halves of tile s + 3 go into them.  The loads for
     // tile s + 3 are issued before waiting for tile s.
