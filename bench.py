@@ -257,6 +257,7 @@ def run_ours(args, rank, world):
         if not args.only_step:
             result["fwd_workloads"] = forward_workloads(fa, torch, tflops_peak, peak_src)
             result["fwd_workloads"].append(forward_fp8_workload(fa, torch, tflops_peak, peak_src))
+            result["bwd_workloads"] = backward_workloads(fa, torch, tflops_peak, peak_src)
             result["e2e"] = end_to_end(fa, torch, w, min(K, 50))
             if world == 1:
                 result["cpu_baseline"] = cpu_baseline(w)
@@ -322,6 +323,46 @@ def forward_workloads(fa, torch, tflops_peak, peak_src):
                     "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst",
                     "input_sets": R})
         del sets, inp
+        torch.cuda.empty_cache()
+    return out
+
+
+# Backward beside the benchmark step: the d = 128 and d = 96 kernel on the
+# causal d = 128 shape's heads (B2 H16 N4096), and the deterministic
+# two-kernel backward on the training shape.
+BWD_WORKLOADS = [
+    ("causal bwd B2 H16 N4096 d128 bf16", (2, 16, 16, 4096, 128), False),
+    ("causal bwd B2 H16 N4096 d96 bf16", (2, 16, 16, 4096, 96), False),
+    ("causal bwd B2 H8 N4096 d64 bf16, deterministic", (2, 8, 8, 4096, 64), True),
+]
+
+
+def backward_workloads(fa, torch, tflops_peak, peak_src):
+    """fa_backward (or fa_backward_deterministic) alone, inputs resident,
+    back-to-back calls; FLOPs 10 B H N^2 d / 2 (causal)."""
+    out = []
+    for name, (B, Hq, Hkv, N, d), det in BWD_WORKLOADS:
+        inp = make_inputs(B, Hq, Hkv, N, d, seed=11, with_grad=True)
+        q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+        scale = 1.0 / math.sqrt(d)
+        o, lse = fa.attention_forward(q, k, v, causal=True, scale=scale)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        call = fa.fa_backward_deterministic if det else fa.fa_backward
+        for _ in range(3):
+            call(q, k, v, o, lse, do, dq, dk, dv, scale, True)
+        reps = 20
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s_ev.record()
+        for _ in range(reps):
+            call(q, k, v, o, lse, do, dq, dk, dv, scale, True)
+        e_ev.record()
+        torch.cuda.synchronize()
+        ms = s_ev.elapsed_time(e_ev) / reps
+        tf = 10.0 * B * Hq * N * N * d / 2 / (ms * 1e-3) / 1e12
+        out.append({"workload": name, "ms": round(ms, 4), "tflops": round(tf, 1),
+                    "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst"})
+        del q, k, v, do, o, lse, dq, dk, dv
         torch.cuda.empty_cache()
     return out
 
