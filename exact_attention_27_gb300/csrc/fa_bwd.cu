@@ -350,19 +350,28 @@ __global__ void __launch_bounds__(192, 1)
       ++wg_phase;
       return __all_sync(0xffffffffu, r);
     };
+    // L log2e and D of query row t of step s (dead rows: L = +inf so P = 0).
+    // Each step's values are loaded one step ahead, so that the global-load
+    // latency is not on the step's critical path.
+    auto load_ld = [&](int s, float& lv, float& dv) {
+      const int g = s / per_head;
+      const int qrow = (i0 + (s - g * per_head)) * C::BQ + t;
+      const bool live = qrow < p.N;
+      const size_t idx = static_cast<size_t>(b * p.Hq + hkv * p.G + g) * p.N + (live ? qrow : 0);
+      lv = live ? p.lse[idx] * kLog2e : INFINITY;
+      dv = live ? p.Dvec[idx] : 0.0f;
+    };
+    float l_cur = 0.0f, d_cur = 0.0f;
+    if (n_steps > 0) load_ld(0, l_cur, d_cur);
     for (int s = 0; s < n_steps; ++s) {
       const int g = s / per_head;
       const int it = i0 + (s - g * per_head);
       const int bhq = b * p.Hq + hkv * p.G + g;
       const int q0 = it * C::BQ;
       const int buf = s & 1;
-      {
-        const int qrow = q0 + t;
-        const bool live = qrow < p.N;
-        const size_t idx = static_cast<size_t>(bhq) * p.N + (live ? qrow : 0);
-        sL[buf * 128 + t] = live ? p.lse[idx] * kLog2e : INFINITY;  // dead rows: P = 0
-        sD[buf * 128 + t] = live ? p.Dvec[idx] : 0.0f;
-      }
+      sL[buf * 128 + t] = l_cur;
+      sD[buf * 128 + t] = d_cur;
+      if (s + 1 < n_steps) load_ld(s + 1, l_cur, d_cur);  // used at the next step
       if (!(ok = wg_sync())) break;
       ok = __all_sync(0xffffffffu,
                       mbar_wait(bar(C::B_SDP), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));
