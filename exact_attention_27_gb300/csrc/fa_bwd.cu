@@ -100,7 +100,12 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float4* __restri
 //                                     into the fp32 dQ accumulator
 // dK is multiplied by scale once at the end; dQ gets its scale in B3.
 //
-// Warp roles (192 threads): warps 0-3 key rows, warp 4 TMA, warp 5 MMA.
+// Warp roles (384 threads): warps 0-3 key rows (P^T, dS^T, L/D, epilogue),
+// warps 4-7 dQ drain, warp 8 TMA, warp 9 MMA, warps 10-11 idle.  The drain
+// warpgroup takes a step's dQ out of TMEM at once (freeing the columns for
+// the next dP^T) and reduces it while the key-row warps go on to the next
+// step.  Registers: 152 for warps 8-11, 200 key rows, 152 drain
+// (128 x (200 + 152 + 152) = 384 x 168, the launch total).
 // Tensor memory: dK [0, DP), dV [DP, 2DP), S^T/P^T 128 columns, dP^T 128
 // columns, dQ 64 columns after dP^T when D = 64, or in dP^T's columns when
 // DP = 128 (DP = D rounded up to a multiple of 64).
@@ -133,12 +138,13 @@ struct BwdCfg {
   static constexpr int B_PDS = B_SDP + 1;         // P^T in TMEM and dS^T in smem (128 arrivals)
   static constexpr int B_DQFULL = B_PDS + 1;      // dQ in TMEM, all MMAs of the step done
   static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ columns drained (128 arrivals)
-  static constexpr int B_WG = B_DQFREE + 1;       // warpgroup-internal sync (128 arrivals)
-  static constexpr int B_DRAIN = B_WG + 1;
+  static constexpr int B_WG = B_DQFREE + 1;       // key-row warpgroup sync (128 arrivals)
+  static constexpr int B_WG2 = B_WG + 1;         // drain warpgroup sync (128 arrivals)
+  static constexpr int B_DRAIN = B_WG2 + 1;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_DK = 0;
   static constexpr uint32_t COL_DV = DP;
@@ -173,7 +179,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // DQ = false builds the dK/dV-only kernel of the deterministic backward.
 template <int D, bool CAUSAL, bool DQ>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
@@ -208,11 +214,12 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQFREE), 128);
     mbar_init(bar(C::B_WG), 128);
+    mbar_init(bar(C::B_WG2), 128);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -228,114 +235,118 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sDS = sbase + C::OFF_DS;
   const uint32_t sSTG = sbase + C::OFF_STG;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
-    if (elect_one()) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE);
-#pragma unroll
-      for (int s = 0; s < C::SUB; ++s) {
-        tma_load_3d(sK + s * C::SUB_BYTES, &tmK, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
-        tma_load_3d(sV + s * C::SUB_BYTES, &tmV, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
-      }
-      int issued = 0;
-      for (int st_i = 0; st_i < n_steps; ++st_i) {
-        const int st = st_i % C::NSQ;
-        if (st_i >= C::NSQ && !mbar_wait(bar(C::B_QDEMPTY + st), ((st_i / C::NSQ) - 1) & 1,
-                                         abort_flag, p.err, kErrTimeoutLoad))
-          break;
-        const int g = st_i / per_head;
-        const int it = i0 + (st_i - g * per_head);
-        const int bhq = b * p.Hq + hkv * p.G + g;
-        mbar_arrive_expect_tx(bar(C::B_QDFULL + st), 2 * C::TILE);
-#pragma unroll
+  if (warp >= 8) {
+    reg_decrease<152>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ TMA producer
+      if (elect_one()) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+        mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE);
+  #pragma unroll
         for (int s = 0; s < C::SUB; ++s) {
-          tma_load_3d(sQ + st * C::TILE + s * C::SUB_BYTES, &tmQ, bar(C::B_QDFULL + st), 64 * s,
-                      it * C::BQ, bhq);
-          tma_load_3d(sdO + st * C::TILE + s * C::SUB_BYTES, &tmdO, bar(C::B_QDFULL + st),
-                      64 * s, it * C::BQ, bhq);
+          tma_load_3d(sK + s * C::SUB_BYTES, &tmK, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
+          tma_load_3d(sV + s * C::SUB_BYTES, &tmV, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
         }
-        issued = st_i + 1;
+        int issued = 0;
+        for (int st_i = 0; st_i < n_steps; ++st_i) {
+          const int st = st_i % C::NSQ;
+          if (st_i >= C::NSQ && !mbar_wait(bar(C::B_QDEMPTY + st), ((st_i / C::NSQ) - 1) & 1,
+                                           abort_flag, p.err, kErrTimeoutLoad))
+            break;
+          const int g = st_i / per_head;
+          const int it = i0 + (st_i - g * per_head);
+          const int bhq = b * p.Hq + hkv * p.G + g;
+          mbar_arrive_expect_tx(bar(C::B_QDFULL + st), 2 * C::TILE);
+  #pragma unroll
+          for (int s = 0; s < C::SUB; ++s) {
+            tma_load_3d(sQ + st * C::TILE + s * C::SUB_BYTES, &tmQ, bar(C::B_QDFULL + st), 64 * s,
+                        it * C::BQ, bhq);
+            tma_load_3d(sdO + st * C::TILE + s * C::SUB_BYTES, &tmdO, bar(C::B_QDFULL + st),
+                        64 * s, it * C::BQ, bhq);
+          }
+          issued = st_i + 1;
+        }
+        if (*abort_flag) {
+          mbar_wait_timed(bar(C::B_KV), 0);
+          for (int s2 = max(0, issued - C::NSQ); s2 < issued; ++s2)
+            mbar_wait_timed(bar(C::B_QDFULL + s2 % C::NSQ), (s2 / C::NSQ) & 1);
+        }
       }
-      if (*abort_flag) {
-        mbar_wait_timed(bar(C::B_KV), 0);
-        for (int s2 = max(0, issued - C::NSQ); s2 < issued; ++s2)
-          mbar_wait_timed(bar(C::B_QDFULL + s2 % C::NSQ), (s2 / C::NSQ) & 1);
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ MMA issuer
+      if (elect_one()) {
+        constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+        constexpr uint32_t id_kd = idesc_bf16_f32(128, C::DP, false, true);  // dV, dK
+        constexpr uint32_t id_q = idesc_bf16_f32(128, C::DP, true, true);    // dQ
+        bool ok = mbar_wait(bar(C::B_KV), 0, abort_flag, p.err, kErrTimeoutMma);
+        for (int s = 0; ok && s < n_steps; ++s) {
+          const int st = s % C::NSQ;
+          const uint32_t q_st = sQ + st * C::TILE;
+          const uint32_t do_st = sdO + st * C::TILE;
+          if (!mbar_wait(bar(C::B_QDFULL + st), (s / C::NSQ) & 1, abort_flag, p.err,
+                         kErrTimeoutMma))
+            break;
+          tc_fence_after();
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+            mma_ss(tmem + C::COL_S, smem_desc_sw128(sK + off, 16, 1024),
+                   smem_desc_sw128(q_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
+          }
+          if (C::DP == 128 && s > 0) {
+            // dQ of the previous step lives in dP^T's columns until drained.
+            if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+            tc_fence_after();
+          }
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+            mma_ss(tmem + C::COL_DP, smem_desc_sw128(sV + off, 16, 1024),
+                   smem_desc_sw128(do_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C::B_SDP));
+          if (!mbar_wait(bar(C::B_PDS), s & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+          tc_fence_after();
+          // dV += P^T dO_i   (A = P^T in TMEM: 16 queries = 8 packed columns per step)
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8,
+                   smem_desc_sw128(do_st + kk * 2048, C::SUB_BYTES, 1024), id_kd,
+                   (s > 0 || kk > 0) ? 1u : 0u);
+          // dK += dS^T Q_i   (A = dS^T K-major: queries contiguous per key row)
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
+            mma_ss(tmem + C::COL_DK, smem_desc_sw128(sDS + off, 16, 1024),
+                   smem_desc_sw128(q_st + kk * 2048, C::SUB_BYTES, 1024), id_kd,
+                   (s > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (D == 64 && s > 0) {
+            if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+            tc_fence_after();
+          }
+          // dQ_i = dS K_j    (A = dS: the dS^T buffer read MN-major; B = K_j MN-major)
+  #pragma unroll
+          for (int kk = 0; kk < (DQ ? 8 : 0); ++kk)
+            mma_ss(tmem + C::COL_DQ, smem_desc_sw128(sDS + kk * 2048, C::SUB_BYTES, 1024),
+                   smem_desc_sw128(sK + kk * 2048, C::SUB_BYTES, 1024), id_q, kk > 0 ? 1u : 0u);
+          mma_commit(bar(C::B_QDEMPTY + st));
+          mma_commit(bar(C::B_DQFULL));
+        }
+        if (*abort_flag) {
+          mma_commit(bar(C::B_DRAIN));
+          mbar_wait_timed(bar(C::B_DRAIN), 0);
+        }
       }
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (elect_one()) {
-      constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t id_kd = idesc_bf16_f32(128, C::DP, false, true);  // dV, dK
-      constexpr uint32_t id_q = idesc_bf16_f32(128, C::DP, true, true);    // dQ
-      bool ok = mbar_wait(bar(C::B_KV), 0, abort_flag, p.err, kErrTimeoutMma);
-      for (int s = 0; ok && s < n_steps; ++s) {
-        const int st = s % C::NSQ;
-        const uint32_t q_st = sQ + st * C::TILE;
-        const uint32_t do_st = sdO + st * C::TILE;
-        if (!mbar_wait(bar(C::B_QDFULL + st), (s / C::NSQ) & 1, abort_flag, p.err,
-                       kErrTimeoutMma))
-          break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S, smem_desc_sw128(sK + off, 16, 1024),
-                 smem_desc_sw128(q_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
-        }
-        if (C::DP == 128 && s > 0) {
-          // dQ of the previous step lives in dP^T's columns until drained.
-          if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_DP, smem_desc_sw128(sV + off, 16, 1024),
-                 smem_desc_sw128(do_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(C::B_SDP));
-        if (!mbar_wait(bar(C::B_PDS), s & 1, abort_flag, p.err, kErrTimeoutMma)) break;
-        tc_fence_after();
-        // dV += P^T dO_i   (A = P^T in TMEM: 16 queries = 8 packed columns per step)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8,
-                 smem_desc_sw128(do_st + kk * 2048, C::SUB_BYTES, 1024), id_kd,
-                 (s > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q_i   (A = dS^T K-major: queries contiguous per key row)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_DK, smem_desc_sw128(sDS + off, 16, 1024),
-                 smem_desc_sw128(q_st + kk * 2048, C::SUB_BYTES, 1024), id_kd,
-                 (s > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (D == 64 && s > 0) {
-          if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
-          tc_fence_after();
-        }
-        // dQ_i = dS K_j    (A = dS: the dS^T buffer read MN-major; B = K_j MN-major)
-#pragma unroll
-        for (int kk = 0; kk < (DQ ? 8 : 0); ++kk)
-          mma_ss(tmem + C::COL_DQ, smem_desc_sw128(sDS + kk * 2048, C::SUB_BYTES, 1024),
-                 smem_desc_sw128(sK + kk * 2048, C::SUB_BYTES, 1024), id_q, kk > 0 ? 1u : 0u);
-        mma_commit(bar(C::B_QDEMPTY + st));
-        mma_commit(bar(C::B_DQFULL));
-      }
-      if (*abort_flag) {
-        mma_commit(bar(C::B_DRAIN));
-        mbar_wait_timed(bar(C::B_DRAIN), 0);
-      }
-    }
-  } else {
+  } else if (warp < 4) {
+    reg_increase<200>();
     // ------------------------------------------------------------ key rows
-    // L and D are read, and dQ reduced into the accumulator, only once the
-    // row-dot pass (the grid before this one) has completed.
+    // L and D are read only once the row-dot pass (the grid before this one)
+    // has completed.
     grid_dependency_wait();
     const int t = threadIdx.x;  // key row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
@@ -363,10 +374,12 @@ __global__ void __launch_bounds__(192, 1)
     };
     float l_cur = 0.0f, d_cur = 0.0f;
     if (n_steps > 0) load_ld(0, l_cur, d_cur);
+    // Step s + 1's dS^T overwrites step s's in shared memory: its S^T/dP^T
+    // are computed only after the drain has read step s's dQ, by which time
+    // every product of step s (the ones reading dS^T too) has completed.
     for (int s = 0; s < n_steps; ++s) {
       const int g = s / per_head;
       const int it = i0 + (s - g * per_head);
-      const int bhq = b * p.Hq + hkv * p.G + g;
       const int q0 = it * C::BQ;
       const int buf = s & 1;
       sL[buf * 128 + t] = l_cur;
@@ -414,46 +427,13 @@ __global__ void __launch_bounds__(192, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_PDS));
-      // ---- drain dQ_i into the fp32 accumulator
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar(C::B_DQFULL), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));
-      if (!ok) break;
-      tc_fence_after();
-      // D / 32 boxes of 128 rows x 32 fp32, two per pass.
-#pragma unroll
-      for (int pass = 0; pass < (DQ ? (D / 32 + 1) / 2 : 0); ++pass) {
-        constexpr int kBoxes = D / 32;
-        const bool second = 2 * pass + 1 < kBoxes;
-        if (t == 0) bulk_wait_group_read0();  // staging free again
-        if (!(ok = wg_sync())) break;
-        uint32_t a[32], bb[32];
-        tmem_ld32(tmem + lane_off + C::COL_DQ + pass * 64, a);
-        if (second) tmem_ld32(tmem + lane_off + C::COL_DQ + pass * 64 + 32, bb);
-        tmem_wait_ld();
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          st_shared_v4(sSTG + sw128(t, ch), a[4 * ch], a[4 * ch + 1], a[4 * ch + 2],
-                       a[4 * ch + 3]);
-          if (second)
-            st_shared_v4(sSTG + C::SUB_BYTES + sw128(t, ch), bb[4 * ch], bb[4 * ch + 1],
-                         bb[4 * ch + 2], bb[4 * ch + 3]);
-        }
-        fence_proxy_async_smem();
-        if (!(ok = wg_sync())) break;
-        if (t == 0) {
-          tma_reduce_add_3d(&tmdQ, sSTG, pass * 64, q0, bhq);
-          if (second) tma_reduce_add_3d(&tmdQ, sSTG + C::SUB_BYTES, pass * 64 + 32, q0, bhq);
-          bulk_commit_group();
-        }
-      }
-      if (!ok) break;
-      tc_fence_before();
-      mbar_arrive(bar(C::B_DQFREE));
     }
-    if (t == 0) bulk_wait_group0();
-    __syncwarp();  // lane 0 waited alone; the TMEM loads below are warp-collective
-    grid_launch_dependents();  // the dQ finalisation may be scheduled
-    // ---- epilogue: dK (times scale) and dV, one key row per thread
+    // ---- epilogue: dK (times scale) and dV, one key row per thread, once the
+    // last step's products have completed (the earlier steps' completed before
+    // the last step's S^T/dP^T were computed, so one phase is outstanding).
+    if (ok && n_steps > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQFULL), (n_steps - 1) & 1, abort_flag,
+                                             p.err, kErrTimeoutEpilogue));
     if (ok) {
       tc_fence_after();
       __nv_bfloat16* dk_row = p.dk + (static_cast<size_t>(kvz) * p.N + (key_live ? key : 0)) * D;
@@ -482,6 +462,72 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
+  } else {
+    reg_decrease<152>();
+    // ------------------------------------------------------------ dQ drain
+    // dQ of step s sits in dP^T's columns: take all of it into registers,
+    // hand the columns back (the next dP^T may be computed), then reduce it
+    // into the fp32 accumulator through the staging tile, D / 32 boxes of
+    // 128 rows x 32 fp32, two per pass.  The accumulator was zeroed by the
+    // row-dot pass (the grid before this one).
+    grid_dependency_wait();
+    const int t = threadIdx.x & 127;  // query row of the step's tile
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t wg_phase = 0;
+    bool ok = true;
+    auto wg_sync = [&]() -> bool {
+      mbar_arrive(bar(C::B_WG2));
+      const bool r = mbar_wait(bar(C::B_WG2), wg_phase & 1, abort_flag, p.err, kErrTimeoutOther);
+      ++wg_phase;
+      return __all_sync(0xffffffffu, r);
+    };
+    constexpr int kBoxes = D / 32;
+    for (int s = 0; s < n_steps; ++s) {
+      const int g = s / per_head;
+      const int it = i0 + (s - g * per_head);
+      const int bhq = b * p.Hq + hkv * p.G + g;
+      const int q0 = it * C::BQ;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::B_DQFULL), s & 1, abort_flag, p.err, kErrTimeoutOther));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dqv[DQ ? kBoxes : 1][32];
+      if (DQ) {
+#pragma unroll
+        for (int x = 0; x < kBoxes; ++x) tmem_ld32(tmem + lane_off + C::COL_DQ + x * 32, dqv[x]);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DQFREE));  // dP^T's columns may be overwritten now
+#pragma unroll
+      for (int pass = 0; pass < (DQ ? (kBoxes + 1) / 2 : 0); ++pass) {
+        const bool second = 2 * pass + 1 < kBoxes;
+        if (t == 0) bulk_wait_group_read0();  // staging free again
+        if (!(ok = wg_sync())) break;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t* a = dqv[2 * pass];
+          st_shared_v4(sSTG + sw128(t, ch), a[4 * ch], a[4 * ch + 1], a[4 * ch + 2],
+                       a[4 * ch + 3]);
+          if (second) {
+            const uint32_t* bb = dqv[2 * pass + 1];
+            st_shared_v4(sSTG + C::SUB_BYTES + sw128(t, ch), bb[4 * ch], bb[4 * ch + 1],
+                         bb[4 * ch + 2], bb[4 * ch + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        if (!(ok = wg_sync())) break;
+        if (t == 0) {
+          tma_reduce_add_3d(&tmdQ, sSTG, pass * 64, q0, bhq);
+          if (second) tma_reduce_add_3d(&tmdQ, sSTG + C::SUB_BYTES, pass * 64 + 32, q0, bhq);
+          bulk_commit_group();
+        }
+      }
+      if (!ok) break;
+    }
+    if (t == 0) bulk_wait_group0();
+    __syncwarp();
+    grid_launch_dependents();  // the dQ finalisation may be scheduled
   }
 
   // Every warp reconverges first: in the TMA and MMA warps only one lane did
@@ -489,7 +535,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
