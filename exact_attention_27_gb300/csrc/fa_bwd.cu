@@ -129,7 +129,7 @@ struct BwdCfg {
   static constexpr int OFF_DO = OFF_Q + NSQ * TILE;
   static constexpr int OFF_DS = OFF_DO + NSQ * TILE;  // dS^T: 128 keys x 128 queries bf16
   static constexpr int OFF_STG = OFF_DS + 2 * SUB_BYTES;  // dQ staging: 2 boxes 128 x 32 fp32
-  static constexpr int OFF_LD = OFF_STG + 2 * SUB_BYTES;  // L log2e [2][128], D [2][128]
+  static constexpr int OFF_LD = OFF_STG + 2 * SUB_BYTES;  // -L log2e [2][128], -D [2][128]
   static constexpr int OFF_BAR = OFF_LD + 4 * 128 * 4;
   static constexpr int B_KV = 0;
   static constexpr int B_QDFULL = 1;
@@ -361,16 +361,17 @@ __global__ void __launch_bounds__(384, 1)
       ++wg_phase;
       return __all_sync(0xffffffffu, r);
     };
-    // L log2e and D of query row t of step s (dead rows: L = +inf so P = 0).
-    // Each step's values are loaded one step ahead, so that the global-load
-    // latency is not on the step's critical path.
+    // -L log2e and -D of query row t of step s (negated, so that the loop
+    // below adds them; dead rows: -L = -inf so P = 0).  Each step's values
+    // are loaded one step ahead, so that the global-load latency is not on
+    // the step's critical path.
     auto load_ld = [&](int s, float& lv, float& dv) {
       const int g = s / per_head;
       const int qrow = (i0 + (s - g * per_head)) * C::BQ + t;
       const bool live = qrow < p.N;
       const size_t idx = static_cast<size_t>(b * p.Hq + hkv * p.G + g) * p.N + (live ? qrow : 0);
-      lv = live ? p.lse[idx] * kLog2e : INFINITY;
-      dv = live ? p.Dvec[idx] : 0.0f;
+      lv = live ? -p.lse[idx] * kLog2e : -INFINITY;
+      dv = live ? -p.Dvec[idx] : 0.0f;
     };
     float l_cur = 0.0f, d_cur = 0.0f;
     if (n_steps > 0) load_ld(0, l_cur, d_cur);
@@ -390,9 +391,11 @@ __global__ void __launch_bounds__(384, 1)
                       mbar_wait(bar(C::B_SDP), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
-      const float* Lb = sL + buf * 128;
-      const float* Db = sD + buf * 128;
-      const bool diag = CAUSAL && (it == jt);
+      const float4* L4b = reinterpret_cast<const float4*>(sL + buf * 128);  // -L log2e
+      const float4* D4b = reinterpret_cast<const float4*>(sD + buf * 128);  // -D
+      // Masking is needed only on the diagonal tile and for keys past N.
+      const bool masked = __any_sync(0xffffffffu, (CAUSAL && it == jt) || !key_live);
+      const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t sv[32], dpv[32];
@@ -401,18 +404,41 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_ld();
         uint32_t pk[16], dk16[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          float pv[2], dsv[2];
+        for (int u4 = 0; u4 < 8; ++u4) {
+          const float4 nl = L4b[cc * 8 + u4];
+          const float4 nd = D4b[cc * 8 + u4];
+          float pv[4];
+          // exp2 argument s c - L log2e on pairs
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * u4]), __uint_as_float(sv[4 * u4 + 1])),
+                           c2, f2_pack(nl.x, nl.y)),
+                    pv[0], pv[1]);
+          f2_unpack(
+              f2_fma(f2_pack(__uint_as_float(sv[4 * u4 + 2]), __uint_as_float(sv[4 * u4 + 3])),
+                     c2, f2_pack(nl.z, nl.w)),
+              pv[2], pv[3]);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int qq = cc * 32 + 2 * u + h;
-            float pr = ex2_approx(fmaf(__uint_as_float(sv[2 * u + h]), c, -Lb[qq]));
-            if (!key_live || (diag && key > q0 + qq)) pr = 0.0f;
-            pv[h] = pr;
-            dsv[h] = pr * (__uint_as_float(dpv[2 * u + h]) - Db[qq]);
+          for (int e = 0; e < 4; ++e) pv[e] = ex2_approx(pv[e]);
+          if (masked) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (!key_live || (CAUSAL && key > q0 + cc * 32 + u4 * 4 + e)) pv[e] = 0.0f;
           }
-          pk[u] = pack_bf16x2(pv[0], pv[1]);
-          dk16[u] = pack_bf16x2(dsv[0], dsv[1]);
+          // dS = P o (dP - D) on pairs
+          const uint64_t ds01 = f2_mul(
+              f2_pack(pv[0], pv[1]),
+              f2_add(f2_pack(__uint_as_float(dpv[4 * u4]), __uint_as_float(dpv[4 * u4 + 1])),
+                     f2_pack(nd.x, nd.y)));
+          const uint64_t ds23 = f2_mul(
+              f2_pack(pv[2], pv[3]),
+              f2_add(f2_pack(__uint_as_float(dpv[4 * u4 + 2]), __uint_as_float(dpv[4 * u4 + 3])),
+                     f2_pack(nd.z, nd.w)));
+          float dsv[4];
+          f2_unpack(ds01, dsv[0], dsv[1]);
+          f2_unpack(ds23, dsv[2], dsv[3]);
+          pk[2 * u4] = pack_bf16x2(pv[0], pv[1]);
+          pk[2 * u4 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dk16[2 * u4] = pack_bf16x2(dsv[0], dsv[1]);
+          dk16[2 * u4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
         // P^T (bf16) over the S^T columns already read: queries cc*32.. -> columns cc*16..
         tmem_st16(tmem + lane_off + C::COL_S + cc * 16, pk);
