@@ -122,23 +122,28 @@ struct BwdCfg {
   static constexpr int SUB = DP / 64;
   static constexpr int SUB_BYTES = 128 * 128;
   static constexpr int TILE = SUB * SUB_BYTES;  // 128 x DP bf16
-  static constexpr int NSQ = (D == 64) ? 2 : 1; // Q / dO stages
+  // Q has two stages, so that S^T of the next step needs no load; dO has one,
+  // released as soon as dV has read it.  dQ leaves through one staging box of
+  // 128 rows x 32 fp32, refilled once the previous reduce has read it.
+  static constexpr int NQ = 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
   static constexpr int OFF_Q = OFF_V + TILE;
-  static constexpr int OFF_DO = OFF_Q + NSQ * TILE;
-  static constexpr int OFF_DS = OFF_DO + NSQ * TILE;  // dS^T: 128 keys x 128 queries bf16
-  static constexpr int OFF_STG = OFF_DS + 2 * SUB_BYTES;  // dQ staging: 2 boxes 128 x 32 fp32
-  static constexpr int OFF_LD = OFF_STG + 2 * SUB_BYTES;  // -L log2e [2][128], -D [2][128]
+  static constexpr int OFF_DO = OFF_Q + NQ * TILE;
+  static constexpr int OFF_DS = OFF_DO + TILE;    // dS^T: 128 keys x 128 queries bf16
+  static constexpr int OFF_STG = OFF_DS + 2 * SUB_BYTES;  // dQ staging: one box 128 x 32 fp32
+  static constexpr int OFF_LD = OFF_STG + SUB_BYTES;     // -L log2e [2][128], -D [2][128]
   static constexpr int OFF_BAR = OFF_LD + 4 * 128 * 4;
   static constexpr int B_KV = 0;
-  static constexpr int B_QDFULL = 1;
-  static constexpr int B_QDEMPTY = B_QDFULL + NSQ;
-  static constexpr int B_SDP = B_QDEMPTY + NSQ;   // S^T and dP^T in TMEM
+  static constexpr int B_QFULL = 1;               // [NQ]
+  static constexpr int B_QEMPTY = B_QFULL + NQ;   // [NQ]
+  static constexpr int B_DOFULL = B_QEMPTY + NQ;
+  static constexpr int B_DOEMPTY = B_DOFULL + 1;
+  static constexpr int B_SDP = B_DOEMPTY + 1;     // S^T and dP^T in TMEM
   static constexpr int B_PDS = B_SDP + 1;         // P^T in TMEM and dS^T in smem (128 arrivals)
   static constexpr int B_DQFULL = B_PDS + 1;      // dQ in TMEM, all MMAs of the step done
   static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ columns drained (128 arrivals)
-  static constexpr int B_WG = B_DQFREE + 1;       // key-row warpgroup sync (128 arrivals)
+  static constexpr int B_WG = B_DQFREE + 1;      // key-row warpgroup sync (128 arrivals)
   static constexpr int B_WG2 = B_WG + 1;         // drain warpgroup sync (128 arrivals)
   static constexpr int B_DRAIN = B_WG2 + 1;
   static constexpr int NBAR = B_DRAIN + 1;
@@ -205,10 +210,12 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_KV), 1);
-    for (int s = 0; s < C::NSQ; ++s) {
-      mbar_init(bar(C::B_QDFULL + s), 1);
-      mbar_init(bar(C::B_QDEMPTY + s), 1);
+    for (int s = 0; s < C::NQ; ++s) {
+      mbar_init(bar(C::B_QFULL + s), 1);
+      mbar_init(bar(C::B_QEMPTY + s), 1);
     }
+    mbar_init(bar(C::B_DOFULL), 1);
+    mbar_init(bar(C::B_DOEMPTY), 1);
     mbar_init(bar(C::B_SDP), 1);
     mbar_init(bar(C::B_PDS), 128);
     mbar_init(bar(C::B_DQFULL), 1);
@@ -250,29 +257,37 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_3d(sK + s * C::SUB_BYTES, &tmK, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
           tma_load_3d(sV + s * C::SUB_BYTES, &tmV, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
         }
-        int issued = 0;
+        // Q of step s into stage s % NQ, dO into its single stage; each waits
+        // for the step that last used its buffer.
+        int q_issued = 0, do_issued = 0;
         for (int st_i = 0; st_i < n_steps; ++st_i) {
-          const int st = st_i % C::NSQ;
-          if (st_i >= C::NSQ && !mbar_wait(bar(C::B_QDEMPTY + st), ((st_i / C::NSQ) - 1) & 1,
-                                           abort_flag, p.err, kErrTimeoutLoad))
-            break;
           const int g = st_i / per_head;
           const int it = i0 + (st_i - g * per_head);
           const int bhq = b * p.Hq + hkv * p.G + g;
-          mbar_arrive_expect_tx(bar(C::B_QDFULL + st), 2 * C::TILE);
+          const int qs = st_i % C::NQ;
+          if (st_i >= C::NQ && !mbar_wait(bar(C::B_QEMPTY + qs), ((st_i / C::NQ) - 1) & 1,
+                                          abort_flag, p.err, kErrTimeoutLoad))
+            break;
+          mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::TILE);
   #pragma unroll
-          for (int s = 0; s < C::SUB; ++s) {
-            tma_load_3d(sQ + st * C::TILE + s * C::SUB_BYTES, &tmQ, bar(C::B_QDFULL + st), 64 * s,
+          for (int s = 0; s < C::SUB; ++s)
+            tma_load_3d(sQ + qs * C::TILE + s * C::SUB_BYTES, &tmQ, bar(C::B_QFULL + qs), 64 * s,
                         it * C::BQ, bhq);
-            tma_load_3d(sdO + st * C::TILE + s * C::SUB_BYTES, &tmdO, bar(C::B_QDFULL + st),
-                        64 * s, it * C::BQ, bhq);
-          }
-          issued = st_i + 1;
+          q_issued = st_i + 1;
+          if (st_i >= 1 && !mbar_wait(bar(C::B_DOEMPTY), (st_i - 1) & 1, abort_flag, p.err,
+                                      kErrTimeoutLoad))
+            break;
+          mbar_arrive_expect_tx(bar(C::B_DOFULL), C::TILE);
+  #pragma unroll
+          for (int s = 0; s < C::SUB; ++s)
+            tma_load_3d(sdO + s * C::SUB_BYTES, &tmdO, bar(C::B_DOFULL), 64 * s, it * C::BQ, bhq);
+          do_issued = st_i + 1;
         }
         if (*abort_flag) {
           mbar_wait_timed(bar(C::B_KV), 0);
-          for (int s2 = max(0, issued - C::NSQ); s2 < issued; ++s2)
-            mbar_wait_timed(bar(C::B_QDFULL + s2 % C::NSQ), (s2 / C::NSQ) & 1);
+          for (int s2 = max(0, q_issued - C::NQ); s2 < q_issued; ++s2)
+            mbar_wait_timed(bar(C::B_QFULL + s2 % C::NQ), (s2 / C::NQ) & 1);
+          if (do_issued > 0) mbar_wait_timed(bar(C::B_DOFULL), (do_issued - 1) & 1);
         }
       }
     } else if (warp == 9) {
@@ -283,11 +298,10 @@ __global__ void __launch_bounds__(384, 1)
         constexpr uint32_t id_q = idesc_bf16_f32(128, C::DP, true, true);    // dQ
         bool ok = mbar_wait(bar(C::B_KV), 0, abort_flag, p.err, kErrTimeoutMma);
         for (int s = 0; ok && s < n_steps; ++s) {
-          const int st = s % C::NSQ;
-          const uint32_t q_st = sQ + st * C::TILE;
-          const uint32_t do_st = sdO + st * C::TILE;
-          if (!mbar_wait(bar(C::B_QDFULL + st), (s / C::NSQ) & 1, abort_flag, p.err,
-                         kErrTimeoutMma))
+          const int qs = s % C::NQ;
+          const uint32_t q_st = sQ + qs * C::TILE;
+          const uint32_t do_st = sdO;
+          if (!mbar_wait(bar(C::B_QFULL + qs), (s / C::NQ) & 1, abort_flag, p.err, kErrTimeoutMma))
             break;
           tc_fence_after();
   #pragma unroll
@@ -296,11 +310,12 @@ __global__ void __launch_bounds__(384, 1)
             mma_ss(tmem + C::COL_S, smem_desc_sw128(sK + off, 16, 1024),
                    smem_desc_sw128(q_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
           }
-          if (C::DP == 128 && s > 0) {
+          if (s > 0) {
             // dQ of the previous step lives in dP^T's columns until drained.
             if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
-            tc_fence_after();
           }
+          if (!mbar_wait(bar(C::B_DOFULL), s & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+          tc_fence_after();
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
@@ -316,6 +331,7 @@ __global__ void __launch_bounds__(384, 1)
             mma_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8,
                    smem_desc_sw128(do_st + kk * 2048, C::SUB_BYTES, 1024), id_kd,
                    (s > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(C::B_DOEMPTY));  // dO_i is not read after dV
           // dK += dS^T Q_i   (A = dS^T K-major: queries contiguous per key row)
   #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -324,16 +340,12 @@ __global__ void __launch_bounds__(384, 1)
                    smem_desc_sw128(q_st + kk * 2048, C::SUB_BYTES, 1024), id_kd,
                    (s > 0 || kk > 0) ? 1u : 0u);
           }
-          if (D == 64 && s > 0) {
-            if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
-            tc_fence_after();
-          }
+          mma_commit(bar(C::B_QEMPTY + qs));  // Q_i is not read after dK
           // dQ_i = dS K_j    (A = dS: the dS^T buffer read MN-major; B = K_j MN-major)
   #pragma unroll
           for (int kk = 0; kk < (DQ ? 8 : 0); ++kk)
             mma_ss(tmem + C::COL_DQ, smem_desc_sw128(sDS + kk * 2048, C::SUB_BYTES, 1024),
                    smem_desc_sw128(sK + kk * 2048, C::SUB_BYTES, 1024), id_q, kk > 0 ? 1u : 0u);
-          mma_commit(bar(C::B_QDEMPTY + st));
           mma_commit(bar(C::B_DQFULL));
         }
         if (*abort_flag) {
@@ -494,7 +506,7 @@ __global__ void __launch_bounds__(384, 1)
     // dQ of step s sits in dP^T's columns: take all of it into registers,
     // hand the columns back (the next dP^T may be computed), then reduce it
     // into the fp32 accumulator through the staging tile, D / 32 boxes of
-    // 128 rows x 32 fp32, two per pass.  The accumulator was zeroed by the
+    // 128 rows x 32 fp32, one at a time.  The accumulator was zeroed by the
     // row-dot pass (the grid before this one).
     grid_dependency_wait();
     const int t = threadIdx.x & 127;  // query row of the step's tile
@@ -526,26 +538,17 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(bar(C::B_DQFREE));  // dP^T's columns may be overwritten now
 #pragma unroll
-      for (int pass = 0; pass < (DQ ? (kBoxes + 1) / 2 : 0); ++pass) {
-        const bool second = 2 * pass + 1 < kBoxes;
+      for (int x = 0; x < (DQ ? kBoxes : 0); ++x) {
         if (t == 0) bulk_wait_group_read0();  // staging free again
         if (!(ok = wg_sync())) break;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint32_t* a = dqv[2 * pass];
-          st_shared_v4(sSTG + sw128(t, ch), a[4 * ch], a[4 * ch + 1], a[4 * ch + 2],
-                       a[4 * ch + 3]);
-          if (second) {
-            const uint32_t* bb = dqv[2 * pass + 1];
-            st_shared_v4(sSTG + C::SUB_BYTES + sw128(t, ch), bb[4 * ch], bb[4 * ch + 1],
-                         bb[4 * ch + 2], bb[4 * ch + 3]);
-          }
-        }
+        for (int ch = 0; ch < 8; ++ch)
+          st_shared_v4(sSTG + sw128(t, ch), dqv[x][4 * ch], dqv[x][4 * ch + 1], dqv[x][4 * ch + 2],
+                       dqv[x][4 * ch + 3]);
         fence_proxy_async_smem();
         if (!(ok = wg_sync())) break;
         if (t == 0) {
-          tma_reduce_add_3d(&tmdQ, sSTG, pass * 64, q0, bhq);
-          if (second) tma_reduce_add_3d(&tmdQ, sSTG + C::SUB_BYTES, pass * 64 + 32, q0, bhq);
+          tma_reduce_add_3d(&tmdQ, sSTG, x * 32, q0, bhq);
           bulk_commit_group();
         }
       }
