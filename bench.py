@@ -171,13 +171,20 @@ def run_ours(args, rank, world):
     sets = [first] + [new_set() for _ in range(R - 1)]
     flops_fwd, flops_bwd = w.fwd_flops(), w.bwd_flops()
 
+    # An event recorded between two kernels stops the second from being
+    # scheduled while the first finishes (each kernel here is launched as a
+    # programmatic dependent of the one before), so per-kernel events go on
+    # every EVENT_EVERY-th timed step only: before and after the forward and
+    # around the backward main kernel.  The other steps run unobserved.
+    EVENT_EVERY = 10
+
     def step(t, ev=None):
         if ev is not None:
             ev[0].record(stream)
         fa.fa_forward(t["q"], t["k"], t["v"], t["o"], t["lse"], w.scale, True)
         if ev is not None:
             ev[1].record(stream)
-            fa.fa_set_backward_events(ev[2], ev[3])
+        fa.fa_set_backward_events(ev[2] if ev else None, ev[3] if ev else None)
         fa.fa_backward(t["q"], t["k"], t["v"], t["o"], t["lse"], t["do"], t["dq"], t["dk"],
                        t["dv"], w.scale, True)
 
@@ -188,7 +195,8 @@ def run_ours(args, rank, world):
         raise RuntimeError("device error during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    n_obs = (K + EVENT_EVERY - 1) // EVENT_EVERY  # observed steps: 0, 10, 20, ...
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_obs)]
     for e in ev:  # create the events (torch creates them on first record)
         for x in e:
             x.record(stream)
@@ -201,7 +209,8 @@ def run_ours(args, rank, world):
         t_wall = time.perf_counter()
         t_start.record(stream)
         for i in range(K):
-            step(sets[(args.warmup + i) % R], ev[i])
+            obs = ev[i // EVENT_EVERY] if i % EVENT_EVERY == 0 else None
+            step(sets[(args.warmup + i) % R], obs)
         t_end.record(stream)
         fa.fa_set_backward_events(None, None)
         torch.cuda.synchronize()
@@ -213,6 +222,9 @@ def run_ours(args, rank, world):
     total_ms = t_start.elapsed_time(t_end)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
     bwd_main_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    # per-step time over blocks of EVENT_EVERY steps (one observed step each)
+    step_ms = [ev[j][0].elapsed_time(ev[j + 1][0]) / EVENT_EVERY for j in range(n_obs - 1)]
+    step_ms.append(ev[n_obs - 1][0].elapsed_time(t_end) / (K - (n_obs - 1) * EVENT_EVERY))
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -246,10 +258,21 @@ def run_ours(args, rank, world):
         "fwd_ms": round(fwd_avg, 5),
         "bwd_ms": round(ms_per_step - fwd_avg, 5),
         "bwd_main_kernel_ms": round(bwd_main_avg, 5),
+        "per_step_ms": {"step": _med_min(step_ms), "fwd": _med_min(fwd_ms),
+                        "bwd_main_kernel": _med_min(bwd_main_ms),
+                        "events": f"forward and backward main kernel timed on every "
+                                  f"{EVENT_EVERY}th step ({n_obs} steps); step over "
+                                  f"{EVENT_EVERY}-step blocks"},
         "roofline": roofline,
         "gpu_launches": 4 * K,
         "wall_s_timed_region": round(t_wall, 4),
     }
+    gpu_out = None
+    if rank == 0 and not args.only_step:
+        result["graph"] = graph_steps(fa, torch, step, sets, flops_fwd + flops_bwd)
+        if world == 1:  # rank 0's inputs are the oracle sample's (seed 0)
+            torch.cuda.synchronize()
+            gpu_out = {n: first[n].double().cpu().numpy() for n in ("o", "lse", "dq", "dk", "dv")}
     del sets, first, base
     torch.cuda.empty_cache()
     if rank == 0:
@@ -260,8 +283,46 @@ def run_ours(args, rank, world):
             result["bwd_workloads"] = backward_workloads(fa, torch, tflops_peak, peak_src)
             result["e2e"] = end_to_end(fa, torch, w, min(K, 50))
             if world == 1:
-                result["cpu_baseline"] = cpu_baseline(w)
+                result["cpu_baseline"] = cpu_baseline(w, gpu_out)
     return result
+
+
+def _med_min(xs):
+    return {"median": round(statistics.median(xs), 5), "min": round(min(xs), 5)}
+
+
+def graph_steps(fa, torch, step, sets, flops, n=100, replays=5):
+    """The benchmark step captured n times into one CUDA graph (cycling
+    through the same rotating input sets) and replayed: device time per step
+    with no host launch overhead between kernels."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step(sets[0])
+            side.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(n):
+                    step(sets[i % len(sets)])
+        torch.cuda.current_stream().wait_stream(side)
+        g.replay()
+        g.replay()
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s_ev.record()
+        for _ in range(replays):
+            g.replay()
+        e_ev.record()
+        torch.cuda.synchronize()
+        if fa.fa_last_device_error() != 0:
+            raise RuntimeError("device error during the graph replays")
+        ms = s_ev.elapsed_time(e_ev) / (replays * n)
+        del g
+        return {"steps_per_graph": n, "replays": replays, "ms_per_step": round(ms, 5),
+                "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s"}
+    except Exception as exc:  # reported, not fatal: the eager numbers stand
+        return {"error": f"{type(exc).__name__}: {exc}"[:200]}
 
 
 def run_forward_only(args):
@@ -465,25 +526,71 @@ def end_to_end(fa, torch, w, K):
 
 # ------------------------------------------------------------------ oracle arms
 
-def oracle_sample(w, q_block, step_index):
+def oracle_sample(w, q_block, step_index, keep=None):
     """Oracle forward + backward for one block of `q_block` query rows in every
     head of the workload (full keys, causal), and the algorithmic FLOPs of the
-    rows processed.  Rows rotate through the sequence from step to step."""
+    rows processed.  Rows rotate through the sequence from step to step,
+    starting with the last block.  If `keep` is a list, the block's first row
+    and the oracle's outputs are appended to it."""
     import oracle
 
     inp = _oracle_inputs(w)
     nblk = w.N // q_block
-    r0 = (step_index * 7919 % nblk) * q_block
+    r0 = ((nblk - 1 + step_index * 7919) % nblk) * q_block
     q = inp["q"][:, :, r0:r0 + q_block]
     do = inp["do"][:, :, r0:r0 + q_block]
     t0 = time.perf_counter()
-    oracle.attention_forward(q, inp["k"], inp["v"], w.scale, True, q_offset=r0)
-    oracle.attention_backward(q, inp["k"], inp["v"], do, w.scale, True, q_offset=r0)
+    fwd = oracle.attention_forward(q, inp["k"], inp["v"], w.scale, True, q_offset=r0)
+    bwd = oracle.attention_backward(q, inp["k"], inp["v"], do, w.scale, True, q_offset=r0)
     dt = time.perf_counter() - t0
+    if keep is not None:
+        keep.append((r0, fwd, bwd))
     keys_seen = sum(i + 1 for i in range(r0, r0 + q_block))  # per head
     heads = w.B * w.Hq
     flops = heads * keys_seen * w.d * (4 + 10)
     return flops, dt
+
+
+# Tolerances of the comparison against the oracle (bf16 inputs, fp32
+# accumulation): O max and mean absolute error, L max absolute error, and
+# each gradient's max absolute error relative to its largest reference value.
+TOL = {"o_max_abs": 2e-2, "o_mean_abs": 2e-3, "lse_max_abs": 1e-3, "grad_rel": 5e-2}
+
+
+def sampled_errors(w, samples, gpu, q_block):
+    """Errors of the GPU outputs `gpu` (o, lse, dq, dk, dv as float arrays)
+    on the oracle's sampled blocks.  Under the causal mask the last block's
+    keys are seen only by that block's queries, so its dK and dV rows are
+    complete and are compared too."""
+    import numpy as np
+    o_err, o_sum, o_n, l_err = 0.0, 0.0, 0, 0.0
+    g_err = {"dq": 0.0, "dk": 0.0, "dv": 0.0}
+    g_ref = {"dq": 0.0, "dk": 0.0, "dv": 0.0}
+    for r0, (o_ref, l_ref), (dq_ref, dk_ref, dv_ref) in samples:
+        rows = slice(r0, r0 + q_block)
+        e = np.abs(gpu["o"][:, :, rows] - o_ref)
+        o_err, o_sum, o_n = max(o_err, e.max()), o_sum + e.sum(), o_n + e.size
+        l_err = max(l_err, np.abs(gpu["lse"][:, :, rows] - l_ref).max())
+        pairs = [("dq", gpu["dq"][:, :, rows], dq_ref)]
+        if r0 + q_block == w.N:
+            pairs += [("dk", gpu["dk"][:, :, rows], dk_ref[:, :, rows]),
+                      ("dv", gpu["dv"][:, :, rows], dv_ref[:, :, rows])]
+        for n, g, r in pairs:
+            g_err[n] = max(g_err[n], np.abs(g - r).max())
+            g_ref[n] = max(g_ref[n], np.abs(r).max())
+    out = {"o_max_abs": float(o_err), "o_mean_abs": float(o_sum / max(o_n, 1)),
+           "lse_max_abs": float(l_err)}
+    for n in g_err:
+        out[f"{n}_rel"] = float(g_err[n] / g_ref[n]) if g_ref[n] > 0 else None
+    ok = (out["o_max_abs"] <= TOL["o_max_abs"] and out["o_mean_abs"] <= TOL["o_mean_abs"]
+          and out["lse_max_abs"] <= TOL["lse_max_abs"]
+          and all(out[f"{n}_rel"] is None or out[f"{n}_rel"] <= TOL["grad_rel"] for n in g_err))
+    out = {k: (round(v, 7) if isinstance(v, float) else v) for k, v in out.items()}
+    out["rows"] = (f"{len(samples)} blocks of {q_block} query rows x {w.B * w.Hq} heads "
+                   f"(dq, o, lse); dk, dv: the last {q_block} keys")
+    out["tolerance"] = TOL
+    out["within_tolerance"] = bool(ok)
+    return out
 
 
 _INPUT_CACHE = {}
@@ -497,20 +604,26 @@ def _oracle_inputs(w):
     return _INPUT_CACHE[w.name]
 
 
-def cpu_baseline(w):
+def cpu_baseline(w, gpu=None):
     """The oracle as it stands on the host cores, on a bounded sample of the
-    workload: forward + backward of 256-row query blocks in all 16 heads."""
+    workload: forward + backward of 256-row query blocks in all 16 heads.
+    With the GPU's outputs for the same inputs (`gpu`), the errors on the
+    sampled rows are reported beside the timing."""
     import oracle
     q_block, flops, secs, steps = 256, 0.0, 0.0, 0
+    samples = [] if gpu is not None else None
     while secs < 10.0 and steps < 64:
-        f, dt = oracle_sample(w, q_block, steps)
+        f, dt = oracle_sample(w, q_block, steps, samples)
         flops += f
         secs += dt
         steps += 1
-    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s",
-            "cores": min(oracle.num_threads(), w.B * w.Hq), "kind": "oracle",
-            "sample": f"{steps} blocks of {q_block} query rows x {w.B * w.Hq} heads, "
-                      f"fwd+bwd against all {w.N} keys (causal), {secs:.1f} s"}
+    out = {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s",
+           "cores": min(oracle.num_threads(), w.B * w.Hq), "kind": "oracle",
+           "sample": f"{steps} blocks of {q_block} query rows x {w.B * w.Hq} heads, "
+                     f"fwd+bwd against all {w.N} keys (causal), {secs:.1f} s"}
+    if gpu is not None:
+        out["gpu_errors_on_sample"] = sampled_errors(w, samples, gpu, q_block)
+    return out
 
 
 def run_reference(args, rank, world):

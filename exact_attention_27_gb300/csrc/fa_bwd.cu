@@ -33,8 +33,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
   constexpr int TPR = (PIECES % 4 == 0 && PIECES % 8 != 0) ? 4 : PIECES;
   constexpr int VPT = PIECES / TPR;
   static_assert(TPR * VPT == PIECES && (TPR & (TPR - 1)) == 0, "row split");
-  // The backward's main kernel, launched as a dependent, may start its own
-  // set-up now; it waits for this grid before reading D or the accumulator.
+  // Launched as a programmatic dependent: O and dO are read only once the
+  // grid before has completed.  The backward's main kernel, launched as this
+  // grid's dependent, may then start its own set-up (it reads only the
+  // inputs before it waits for this grid, and D and the accumulator after).
+  grid_dependency_wait();
   grid_launch_dependents();
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = tid / TPR;
@@ -72,9 +75,12 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float4* __restri
                                                           float scale) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   grid_dependency_wait();  // the accumulator is complete once the main kernel is
+  grid_launch_dependents();
   if (i >= n8) return;
+  // L2 loads: the accumulator was written by the grid before, which ran
+  // while this one was already resident.
   const float4 a = __ldcg(acc + 2 * i);
-  const float4 b = __ldg(acc + 2 * i + 1);
+  const float4 b = __ldcg(acc + 2 * i + 1);
   dq[i] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
                      pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
 }
@@ -579,16 +585,16 @@ cudaError_t launch_preprocess(const void* o, const void* dO, float* Dout, long l
   const long long threads = rows * (d == 96 ? 4 : d / 8);  // threads per row as in the kernel
   const long long blocks = (threads + 255) / 256;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(blocks)), block(256);
+  const uint4* o4 = static_cast<const uint4*>(o);
+  const uint4* dO4 = static_cast<const uint4*>(dO);
   if (d == 64)
-    preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows, acc);
-  else if (d == 96)
-    preprocess_kernel<96><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows, acc);
-  else
-    preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), Dout, rows, acc);
-  return cudaGetLastError();
+    return launch_dependent(preprocess_kernel<64>, grid, block, 0, stream, o4, dO4, Dout, rows,
+                            acc);
+  if (d == 96)
+    return launch_dependent(preprocess_kernel<96>, grid, block, 0, stream, o4, dO4, Dout, rows,
+                            acc);
+  return launch_dependent(preprocess_kernel<128>, grid, block, 0, stream, o4, dO4, Dout, rows, acc);
 }
 
 cudaError_t launch_dq_finalize(const float* dq_acc, void* dq, long long n, float scale,

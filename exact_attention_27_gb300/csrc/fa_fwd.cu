@@ -196,6 +196,11 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent of the grid before it in the
+  // stream: Q, K and V are read, and O and L written, only once that grid
+  // has completed; the grid after this one may be scheduled from then on.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   const uint32_t sQ = sbase + C::OFF_Q;
   const uint32_t sK = sbase + C::OFF_K;
@@ -641,8 +646,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   }
   const long long grid = static_cast<long long>(s.B) * s.Hq * p.n_qpairs;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS), C::SMEM_BYTES,
+                          stream, tq, tk, tv, p);
 }
 
 // Query rows per CTA: 128 (fa_fwd_tile1.cu) or 256 (two tiles here); 0 lets

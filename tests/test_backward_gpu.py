@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from parity import check_forward, check_grads
+from parity import GRAD_REL, check_forward, check_grads
 from workloads import WORKLOADS, as_f64, make_inputs, workload_inputs
 
 pytestmark = pytest.mark.gpu
@@ -157,3 +157,46 @@ def test_deterministic_backward_is_bitwise_reproducible(d, G):
     for a, b in zip(g1, g2):
         assert torch.equal(a, b)
     assert torch.equal(g1[1], g3[1]) and torch.equal(g1[2], g3[2])
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,det", [
+    (2, 16, 16, 4096, 128, False),   # the d = 128 backward timed beside the step
+    (2, 16, 16, 4096, 96, False),    # the d = 96 one
+    (1, 8, 2, 4096, 128, False),     # grouped-query heads at full length
+    (2, 16, 16, 4096, 128, True),    # the deterministic path at the same size
+])
+def test_full_size_backward_sampled(B, Hq, Hkv, N, d, det):
+    """Full-size causal backward against the oracle on two 256-row query
+    blocks (the first and the last).  Under the causal mask the last 256 keys
+    are seen only by the last 256 queries, so the oracle's backward of that
+    block gives their dK and dV completely; dQ of both blocks is complete
+    too.  Bounds: the forward's, and 5e-2 x max |reference| over each sampled
+    gradient block."""
+    import exact_attention_27_gb300 as fa
+    inp = make_inputs(B, Hq, Hkv, N, d, seed=11, with_grad=True)
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=scale)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, causal=True, scale=scale,
+                                       deterministic=det)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == 0
+    f = {n: as_f64(inp[n]) for n in ("q", "k", "v", "do")}
+    blk = 256
+    for r0 in (0, N - blk):
+        rows = slice(r0, r0 + blk)
+        o_ref, l_ref = oracle.attention_forward(f["q"][:, :, rows], f["k"], f["v"], scale, True,
+                                                q_offset=r0)
+        check_forward(o[:, :, rows], lse[:, :, rows], o_ref, l_ref, f"forward rows {r0}..")
+        dq_ref, dk_ref, dv_ref = oracle.attention_backward(f["q"][:, :, rows], f["k"], f["v"],
+                                                           f["do"][:, :, rows], scale, True,
+                                                           q_offset=r0)
+        got, ref = [dq[:, :, rows]], [dq_ref]
+        if r0 == N - blk:
+            got += [dk[:, :, rows], dv[:, :, rows]]
+            ref += [dk_ref[:, :, rows], dv_ref[:, :, rows]]
+        for g, r in zip(got, ref):
+            g = g.float().cpu().numpy().astype(np.float64)
+            assert np.isfinite(g).all()
+            err = np.abs(g - r).max()
+            assert err <= GRAD_REL * np.abs(r).max(), f"rows {r0}..: err {err:.3e}"
