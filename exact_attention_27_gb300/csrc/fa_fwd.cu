@@ -19,7 +19,9 @@
 //   warp 9     MMA issuer (one thread) and TMEM owner, in the order
 //              S_A(0) S_B(0), then per key tile j:
 //              O_A += P_A V_j, S_A(j+1) = Q_A K_{j+1}^T, O_B += P_B V_j, S_B(j+1)
-//              (S: A and B from shared memory; O: A = P from tensor memory).
+//              (S: A and B from shared memory; O: A = P from tensor memory);
+//              at D = 64: S_A(0) S_B(0) S_A(1), then per key tile j:
+//              O_A += P_A V_j, S_B(j+1), O_B += P_B V_j, S_A(j+2).
 // Registers: launched at 168 per thread; the third warpgroup gives most of
 // its share to the two softmax warpgroups (56 / 224 / 224: 128 x (224 + 224
 // + 56) = 384 x 168, the launch total).
@@ -29,6 +31,9 @@
 //   columns 128..255  S of tile B
 //   columns 256..256+2DP-1  O accumulators of tiles A and B (fp32; DP = D
 //              rounded up to a multiple of 64)
+// except at D = 64, where three S buffers (columns 0..383) rotate between
+// the two tiles and O_A, O_B sit at 384 and 448: a tile's next S is then
+// computed while its softmax still works on the current one.
 //
 // Online softmax ("L'attention fusionnee", section "Le softmax en ligne"):
 // per key tile m' = max(m, max s), p = exp(s - m'), l = l e^(m - m') + sum p,
@@ -96,22 +101,23 @@ struct FwdCfg {
   static constexpr int B_KEMPTY = B_KFULL + NS;
   static constexpr int B_VFULL = B_KEMPTY + NS;
   static constexpr int B_VEMPTY = B_VFULL + NS;
-  static constexpr int B_SFULL = B_VEMPTY + NS;  // [2] per query tile
-  static constexpr int B_PFULL = B_SFULL + 2;    // [2] per query tile (4 warp arrivals)
+  // At DP = 64 three S buffers of 128 columns rotate between the two tiles
+  // (the n-th S issued goes to buffer n % 3; P overwrites the first 64
+  // columns of its own S), which with the two O accumulators fills the 512
+  // columns; the MMA issuer's order makes each reuse safe.  Otherwise each
+  // tile has its own S columns.
+  static constexpr bool ROT3 = (DP == 64) && !FP8;
+  static constexpr int NSB = ROT3 ? 3 : 2;       // S buffers
+  static constexpr int B_SFULL = B_VEMPTY + NS;  // [NSB] S in buffer (ROT3) or of tile x
+  static constexpr int B_PFULL = B_SFULL + NSB;  // [2] per query tile (4 warp arrivals)
   static constexpr int B_ODONE = B_PFULL + 2;    // [2] per query tile
-  static constexpr int B_SFREE = B_ODONE + 2;    // [2] S of a tile loaded by its softmax (SEP_P)
-  static constexpr int B_DRAIN = B_SFREE + 2;    // abort path: MMAs in flight
+  static constexpr int B_DRAIN = B_ODONE + 2;    // abort path: MMAs in flight
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort word
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O = 256;         // O of tile x at 256 + x * DP
-  // At DP = 64 the 128 columns after the two O accumulators hold P (bf16) of
-  // each tile, so S_x(j+1) can be computed into S_x while the softmax still
-  // works on P_x(j).  At DP = 128 P overwrites S.
-  static constexpr bool SEP_P = (DP == 64) && !FP8;
-  static constexpr uint32_t COL_P = 384;         // SEP_P: P of tile x at 384 + 64 x
+  static constexpr uint32_t COL_O = ROT3 ? 384 : 256;  // O of tile x at COL_O + x * DP
 };
 
 struct FwdParams {
@@ -178,11 +184,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::B_VFULL + s), 1);
       mbar_init(bar(C::B_VEMPTY + s), 1);
     }
+    for (int x = 0; x < C::NSB; ++x) mbar_init(bar(C::B_SFULL + x), 1);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(C::B_SFULL + x), 1);
       mbar_init(bar(C::B_PFULL + x), 4);  // one arrival per softmax warp of the tile
       mbar_init(bar(C::B_ODONE + x), 1);
-      mbar_init(bar(C::B_SFREE + x), 4);  // one arrival per softmax warp of the tile
     }
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -274,9 +279,9 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t v_desc = smem_desc_sw128(sV, FP8 ? 16 : C::SUB_BYTES, 1024);
       const int nx[2] = {nA, nB};
       bool ok = mbar_wait(bar(C::B_QFULL), 0, abort_flag, p.err, kErrTimeoutMma);
-      // S_x(j) = Q_x K_j^T into tile x's S columns.
-      auto issue_s = [&](int x, int j) {
-        const uint32_t d_tmem = tmem + x * 128;
+      // S_x(j) = Q_x K_j^T into S buffer `buf`.
+      auto issue_s = [&](int x, int j, int buf) {
+        const uint32_t d_tmem = tmem + buf * 128;
         const uint64_t qd = desc_add(q_desc, x * C::TILE);
         const uint64_t kd = desc_add(k_desc, (j % C::NS) * C::TILE);
         if constexpr (FP8) {
@@ -293,7 +298,7 @@ __global__ void __launch_bounds__(384, 1)
             mma_ss_k<ID_S, 1>(d_tmem, desc_add(qd, off), desc_add(kd, off));
           }
         }
-        mma_commit(bar(C::B_SFULL + x));
+        mma_commit(bar(C::B_SFULL + buf));
       };
       // K_j is used by the S products of both tiles; wait for it once and
       // release it after its last use.
@@ -304,63 +309,67 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         return true;
       };
-      if (ok && n_kv > 0) {
+      if (!C::ROT3 && ok && n_kv > 0) {
         ok = issue_s_both(0);
         if (ok) {
-          if (nA > 0) issue_s(0, 0);
-          if (nB > 0) issue_s(1, 0);
+          if (nA > 0) issue_s(0, 0, 0);
+          if (nB > 0) issue_s(1, 0, 1);
           mma_commit(bar(C::B_KEMPTY + 0));
         }
       }
-      if constexpr (C::SEP_P) {
-        // Per key tile j: S_A(j+1), S_B(j+1), each once its tile's softmax
-        // has loaded S(j) (they then run under that softmax), then
-        // O_A += P_A V_j and O_B += P_B V_j as the P tiles arrive.
-        for (int j = 0; ok && j < n_kv; ++j) {
+      if constexpr (C::ROT3) {
+        // Three S buffers rotate between the tiles.  S issue order is A0 B0
+        // A1 B1 ..., so S_x(j) is the n-th S issued, n = min(j + x, nA) +
+        // min(j, nB), and goes to buffer n % 3.  Order: S_A(0) S_B(0) S_A(1),
+        // then per key tile j: O_A += P_A V_j, S_B(j+1), O_B += P_B V_j,
+        // S_A(j+2).  Each S then follows the P V of the S that held its buffer
+        // before (number n - 3), and the tensor pipe runs in issue order, so
+        // that P is read before it is overwritten; the softmax of a tile finds
+        // its next S computed while it works on the current one.
+        auto sbuf = [&](int x, int j) { return (min(j + x, nA) + min(j, nB)) % 3; };
+        int k_waited = 0;  // K tiles waited for (first uses come in order)
+        auto s3 = [&](int x, int j) -> bool {
+          if (j >= k_waited) {
+            if (!issue_s_both(j)) return false;
+            k_waited = j + 1;
+          }
+          issue_s(x, j, sbuf(x, j));
+          if (x == 1 || j >= nB) mma_commit(bar(C::B_KEMPTY + j % C::NS));  // K_j's last use
+          return true;
+        };
+        auto pv3 = [&](int x, int j) -> bool {
           const int st = j % C::NS;
-          if (j + 1 < n_kv) {
-            if (!issue_s_both(j + 1)) break;
-#pragma unroll 1
-            for (int x = 0; x < 2; ++x) {
-              if (j + 1 >= nx[x]) continue;
-              if (!mbar_wait(bar(C::B_SFREE + x), j & 1, abort_flag, p.err, kErrTimeoutMma)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              issue_s(x, j + 1);
-            }
-            if (!ok) break;
-            mma_commit(bar(C::B_KEMPTY + (j + 1) % C::NS));
-          }
-          if (!mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err,
-                         kErrTimeoutMma))
-            break;
-#pragma unroll 1
-          for (int x = 0; x < 2; ++x) {
-            if (j >= nx[x]) continue;
-            if (!mbar_wait(bar(C::B_PFULL + x), j & 1, abort_flag, p.err, kErrTimeoutMma)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t vd = desc_add(v_desc, st * C::TILE);
-            const uint32_t pa = tmem + C::COL_P + x * 64;
-            const uint32_t od = tmem + C::COL_O + x * C::DP;
-            if (j == 0)
-              mma_ts_k<ID_O, 0>(od, pa, vd);
-            else
-              mma_ts_k<ID_O, 1>(od, pa, vd);
+          if ((x == 0 || j >= nA) &&
+              !mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
+            return false;
+          if (!mbar_wait(bar(C::B_PFULL + x), j & 1, abort_flag, p.err, kErrTimeoutMma))
+            return false;
+          tc_fence_after();
+          const uint64_t vd = desc_add(v_desc, st * C::TILE);
+          const uint32_t pa = tmem + sbuf(x, j) * 128;  // P packed over its S
+          const uint32_t od = tmem + C::COL_O + x * C::DP;
+          if (j == 0)
+            mma_ts_k<ID_O, 0>(od, pa, vd);
+          else
+            mma_ts_k<ID_O, 1>(od, pa, vd);
 #pragma unroll
-            for (int kk = 1; kk < 8; ++kk)
-              mma_ts_k<ID_O, 1>(od, pa + kk * 8, desc_add(vd, kk * 2048));
-            mma_commit(bar(C::B_ODONE + x));
-          }
-          if (!ok) break;
-          mma_commit(bar(C::B_VEMPTY + st));
+          for (int kk = 1; kk < 8; ++kk)
+            mma_ts_k<ID_O, 1>(od, pa + kk * 8, desc_add(vd, kk * 2048));
+          mma_commit(bar(C::B_ODONE + x));
+          if (x == 1 || j >= nB) mma_commit(bar(C::B_VEMPTY + st));  // V_j's last use
+          return true;
+        };
+        if (ok && nA > 0) ok = s3(0, 0);
+        if (ok && nB > 0) ok = s3(1, 0);
+        if (ok && nA > 1) ok = s3(0, 1);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          if (j < nA && !(ok = pv3(0, j))) break;
+          if (j + 1 < nB && !(ok = s3(1, j + 1))) break;
+          if (j < nB && !(ok = pv3(1, j))) break;
+          if (j + 2 < nA && !(ok = s3(0, j + 2))) break;
         }
       }
-      for (int j = 0; !C::SEP_P && ok && j < n_kv; ++j) {
+      for (int j = 0; !C::ROT3 && ok && j < n_kv; ++j) {
         const int st = j % C::NS;
         if (!mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
           break;
@@ -405,7 +414,7 @@ __global__ void __launch_bounds__(384, 1)
               }
               k_ready = true;
             }
-            issue_s(x, j + 1);
+            issue_s(x, j + 1, x);
           }
         }
         if (!ok) break;
@@ -428,9 +437,7 @@ __global__ void __launch_bounds__(384, 1)
     const int qt = 2 * pair + x;
     const int qi = qt * C::BM + row;
     const int nt = x == 0 ? nA : nB;
-    const uint32_t col_s = x * 128;
     const uint32_t col_o = C::COL_O + x * C::DP;
-    const uint32_t col_p = C::SEP_P ? C::COL_P + x * 64 : col_s;  // P as packed bf16
     const float c = p.scale_log2;
     float m_used = -INFINITY;  // reference maximum, log2 domain
     float l = 0.0f;
@@ -438,8 +445,15 @@ __global__ void __launch_bounds__(384, 1)
     for (int j = 0; j < nt; ++j) {
       // Waits are made warp-uniform: the TMEM loads and stores below are
       // warp-collective, so either every lane goes on or every lane stops.
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + x), j & 1, abort_flag, p.err,
-                                             kErrTimeoutSoftmax));
+      // S_x(j): with ROT3 the n-th S issued, in buffer n % 3 (its (n / 3)-th
+      // use); otherwise tile x's own columns.  P is stored over it as bf16
+      // (e4m3 for FP8).
+      const int sn = C::ROT3 ? min(j + x, nA) + min(j, nB) : 0;
+      const int sb = C::ROT3 ? sn % 3 : x;
+      const uint32_t col_s = sb * 128;
+      const uint32_t col_p = col_s;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + sb), C::ROT3 ? (sn / 3) & 1 : j & 1,
+                                             abort_flag, p.err, kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
       // The row's 128 scores: four loads in flight, one wait.
@@ -453,11 +467,6 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int t = 0; t < 128; ++t) s[t] = __uint_as_float(r[t]);
-      }
-      if constexpr (C::SEP_P) {
-        // S_x is in registers: the next S may be computed into its columns.
-        tc_fence_before();
-        mbar_arrive_warp(bar(C::B_SFREE + x));
       }
       const int kbase = j * C::BN;
       const int qpos = p.q_offset + qi;  // absolute position of this row
@@ -495,9 +504,6 @@ __global__ void __launch_bounds__(384, 1)
       uint64_t ps2[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) ps2[u] = 0ull;
-      // The whole row of P is formed in registers before it is stored, so the
-      // wait below for the previous O += P V (whose P columns these are when
-      // SEP_P) comes after the exponentials rather than before them.
       if constexpr (FP8) {
         // P rounded to e4m3, four keys per TMEM column (the lowest key in the
         // lowest byte); the running sum uses the fp32 values.
@@ -525,16 +531,6 @@ __global__ void __launch_bounds__(384, 1)
           ps2[t & 3] = f2_add(ps2[t & 3], f2_pack(p0, p1));
           pk[t] = pack_bf16x2(p0, p1);
         }
-        if constexpr (C::SEP_P) {
-          // P_x(j) goes where O += P_x(j-1) V reads from: wait for that product
-          // (it also has to be done before O is rescaled below).
-          if (j > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
-                                                   p.err, kErrTimeoutSoftmax));
-            if (!ok) break;
-            tc_fence_after();
-          }
-        }
         tmem_st32(tmem + lane_off + col_p, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
         tmem_st32(tmem + lane_off + col_p + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       }
@@ -542,25 +538,26 @@ __global__ void __launch_bounds__(384, 1)
       f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), sum, sum_hi);
       sum += sum_hi;
       l = l * alpha + sum;
-      if (j > 0) {
-        // O holds P_0..P_{j-1} contributions; it must be final before rescaling
-        // (with SEP_P this was waited for before P was stored).
-        if (!C::SEP_P) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
-                                                 p.err, kErrTimeoutSoftmax));
-          if (!ok) break;
-        }
-        if (__any_sync(0xffffffffu, upd)) {
-          tc_fence_after();
+      // O holds P_0..P_{j-1} contributions; it must be final before it is
+      // rescaled.  With ROT3 nothing else waits for it, so the wait is made
+      // only when a rescale is due (O += P_x(j) V waits for this tile's P, so
+      // the barrier cannot run two phases ahead).
+      const bool resc = j > 0 && __any_sync(0xffffffffu, upd);
+      if (j > 0 && (resc || !C::ROT3)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
+                                               p.err, kErrTimeoutSoftmax));
+        if (!ok) break;
+      }
+      if (resc) {
+        tc_fence_after();
 #pragma unroll
-          for (int q4 = 0; q4 < D / 32; ++q4) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_off + col_o + q4 * 32, r);
-            tmem_wait_ld();
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + col_o + q4 * 32, r);
+          tmem_wait_ld();
 #pragma unroll
-            for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
-            tmem_st32(tmem + lane_off + col_o + q4 * 32, r);
-          }
+          for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
+          tmem_st32(tmem + lane_off + col_o + q4 * 32, r);
         }
       }
       tmem_wait_st();
