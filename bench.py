@@ -464,48 +464,68 @@ def forward_fp8_workload(fa, torch, tflops_peak, peak_src):
 def end_to_end(fa, torch, w, K):
     """Same step through the public API with the inputs in pinned host memory:
     every step copies its q, k, v, dO host->device and reads its o, lse, dq,
-    dk, dv back device->host, all inside the timed region.  The loop is
-    pipelined as a training or serving loop would be: two sets of device
+    dk, dv back device->host, all inside the timed region.  The inputs sit
+    in one pinned host buffer and the outputs in one device buffer (views of
+    each), so a step makes one copy in each direction.  The loop is
+    pipelined as a training or serving loop would be: three sets of device
     buffers and three streams, so that step i+1's inputs go up and step
     i-1's results come down while step i computes (each copy waits only for
     the step that last used its buffers)."""
     inp = make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, seed=1, with_grad=True)
-    h = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+    names = ("q", "k", "v", "do")
+
+    def carve(buf, specs):
+        """Views of a flat byte buffer: (name, shape, dtype) in order."""
+        out, off = {}, 0
+        for n, shape, dt in specs:
+            nb = math.prod(shape) * torch.tensor([], dtype=dt).element_size()
+            out[n] = buf[off:off + nb].view(dt).view(shape)
+            off += nb
+        return out
+
+    in_specs = [(n, tuple(inp[n].shape), inp[n].dtype) for n in names]
+    q_shape, kv_shape = tuple(inp["q"].shape), tuple(inp["k"].shape)
+    out_specs = [("o", q_shape, torch.bfloat16), ("dq", q_shape, torch.bfloat16),
+                 ("dk", kv_shape, torch.bfloat16), ("dv", kv_shape, torch.bfloat16),
+                 ("lse", q_shape[:-1], torch.float32)]
+    nb_in = sum(math.prod(sh) * 2 for _, sh, _ in in_specs)
+    nb_out = sum(math.prod(sh) * (4 if dt == torch.float32 else 2) for _, sh, dt in out_specs)
+    h_in = torch.empty(nb_in, dtype=torch.uint8).pin_memory()
+    hv = carve(h_in, in_specs)
+    for n in names:
+        hv[n].copy_(inp[n])
 
     def buffers():
-        d = {n: torch.empty_like(h[n], device="cuda") for n in h}
-        outs = [torch.empty_like(d["q"]),
-                torch.empty(d["q"].shape[:-1], dtype=torch.float32, device="cuda"),
-                torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])]
-        outs_h = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
-        ev = {k: torch.cuda.Event() for k in ("in", "cmp", "out")}
-        return {"d": d, "outs": outs, "outs_h": outs_h, "ev": ev}
+        d_in = torch.empty(nb_in, dtype=torch.uint8, device="cuda")
+        d_out = torch.empty(nb_out, dtype=torch.uint8, device="cuda")
+        return {"d_in": d_in, "d_out": d_out, "i": carve(d_in, in_specs),
+                "o": carve(d_out, out_specs),
+                "h_out": torch.empty(nb_out, dtype=torch.uint8).pin_memory(),
+                "ev": {k: torch.cuda.Event() for k in ("in", "cmp", "out")}}
 
-    sets = [buffers(), buffers()]
-    h2d = sum(t.numel() * t.element_size() for t in h.values())
-    d2h = sum(t.numel() * t.element_size() for t in sets[0]["outs"])
+    NSET = 3
+    sets = [buffers() for _ in range(NSET)]
     s_cmp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def step(i):
-        S = sets[i % 2]
-        d, (o, lse, dq, dk, dv), ev = S["d"], S["outs"], S["ev"]
+        S = sets[i % NSET]
+        d, o, ev = S["i"], S["o"], S["ev"]
         with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(ev["cmp"])  # step i-2 is done with these inputs
-            for n in h:
-                d[n].copy_(h[n], non_blocking=True)
+            if i >= NSET:
+                s_in.wait_event(ev["cmp"])  # step i-NSET is done with these inputs
+            S["d_in"].copy_(h_in, non_blocking=True)
             ev["in"].record(s_in)
         s_cmp.wait_event(ev["in"])
-        if i >= 2:
-            s_cmp.wait_event(ev["out"])  # step i-2's results have been read
-        fa.fa_forward(d["q"], d["k"], d["v"], o, lse, w.scale, True)
-        fa.fa_backward(d["q"], d["k"], d["v"], o, lse, d["do"], dq, dk, dv, w.scale, True)
+        if i >= NSET:
+            s_cmp.wait_event(ev["out"])  # step i-NSET's results have been read
+        fa.fa_forward(d["q"], d["k"], d["v"], o["o"], o["lse"], w.scale, True)
+        fa.fa_backward(d["q"], d["k"], d["v"], o["o"], o["lse"], d["do"], o["dq"], o["dk"],
+                       o["dv"], w.scale, True)
         ev["cmp"].record(s_cmp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev["cmp"])
-            for src, dst in zip(S["outs"], S["outs_h"]):
-                dst.copy_(src, non_blocking=True)
+            S["h_out"].copy_(S["d_out"], non_blocking=True)
             ev["out"].record(s_out)
 
     for i in range(4):
@@ -513,15 +533,18 @@ def end_to_end(fa, torch, w, K):
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(s_in)
+    t_host = time.perf_counter()
     for i in range(K):
         step(i)
+    t_host = time.perf_counter() - t_host
     stop.record(s_out)
     stop.synchronize()  # the host holds every step's results
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / K
     return {"value": round((w.fwd_flops() + w.bwd_flops()) / (ms * 1e-3) / 1e12, 2),
-            "unit": "TFLOP/s", "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "pipelined": "2 buffer sets, 3 streams"}
+            "unit": "TFLOP/s", "ms_per_step": round(ms, 4), "h2d_bytes_per_step": nb_in,
+            "d2h_bytes_per_step": nb_out, "host_enqueue_ms_per_step": round(t_host * 1e3 / K, 4),
+            "pipelined": f"{NSET} buffer sets, 3 streams, one copy each way per step"}
 
 
 # ------------------------------------------------------------------ oracle arms
