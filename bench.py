@@ -325,6 +325,35 @@ def graph_steps(fa, torch, step, sets, flops, n=100, replays=5):
         return {"error": f"{type(exc).__name__}: {exc}"[:200]}
 
 
+def run_backward_only(args):
+    """fa_backward (or the deterministic one) alone on one backward workload,
+    after one forward for O and L (used for kernel profiles)."""
+    import torch
+    import exact_attention_27_gb300 as fa
+    from exact_attention_27_gb300 import _build
+    _build.build()
+    name, (B, Hq, Hkv, N, d), det = BWD_WORKLOADS[BWD_NAMES[args.backward_only]]
+    inp = make_inputs(B, Hq, Hkv, N, d, seed=11, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    call = fa.fa_backward_deterministic if det else fa.fa_backward
+    for _ in range(args.warmup):
+        call(q, k, v, o, lse, do, dq, dk, dv, scale, True)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        call(q, k, v, o, lse, do, dq, dk, dv, scale, True)
+    e.record()
+    torch.cuda.synchronize()
+    if fa.fa_last_device_error() != 0:
+        raise RuntimeError("device error")
+    ms = s.elapsed_time(e) / args.steps
+    return {"workload": name, "launches": args.warmup + args.steps, "ms": round(ms, 4),
+            "tflops": round(10.0 * B * Hq * N * N * d / 2 / (ms * 1e-3) / 1e12, 1)}
+
+
 def run_forward_only(args):
     """fa_forward alone on one workload (used for kernel profiles)."""
     import torch
@@ -396,6 +425,9 @@ BWD_WORKLOADS = [
     ("causal bwd B2 H16 N4096 d96 bf16", (2, 16, 16, 4096, 96), False),
     ("causal bwd B2 H8 N4096 d64 bf16, deterministic", (2, 8, 8, 4096, 64), True),
 ]
+# Short names for --backward-only.
+BWD_NAMES = {"causal_bwd_n4096_d128": 0, "causal_bwd_n4096_d96": 1,
+             "causal_bwd_det_n4096_d64": 2}
 
 
 def backward_workloads(fa, torch, tflops_peak, peak_src):
@@ -699,6 +731,8 @@ def main():
                     help="time the step only (no extra workloads, e2e or CPU baseline)")
     ap.add_argument("--forward-only", choices=sorted(WORKLOADS), default=None,
                     help="run fa_forward alone on one workload (for kernel profiles)")
+    ap.add_argument("--backward-only", choices=sorted(BWD_NAMES), default=None,
+                    help="run fa_backward alone on one backward workload (for kernel profiles)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -708,6 +742,9 @@ def main():
         ap.error("--gpus must match the launcher's WORLD_SIZE")
     if args.forward_only:
         print(json.dumps(run_forward_only(args)), flush=True)
+        return
+    if args.backward_only:
+        print(json.dumps(run_backward_only(args)), flush=True)
         return
     if args.impl == "reference":
         if rank == 0:
