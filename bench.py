@@ -291,6 +291,47 @@ def _med_min(xs):
     return {"median": round(statistics.median(xs), 5), "min": round(min(xs), 5)}
 
 
+def per_launch_ms(torch, launch, reps=10):
+    """Median and min of `reps` launches, each bracketed by its own events
+    (which also keeps it from overlapping its neighbours)."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for i in range(reps):
+        ev[i][0].record()
+        launch(i)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    return _med_min([a.elapsed_time(b) for a, b in ev])
+
+
+def graph_launches(torch, launch, n=100, replays=5):
+    """`n` launches captured into one CUDA graph and replayed: ms per launch."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            launch(0)
+            side.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(n):
+                    launch(i)
+        torch.cuda.current_stream().wait_stream(side)
+        g.replay()
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s_ev.record()
+        for _ in range(replays):
+            g.replay()
+        e_ev.record()
+        torch.cuda.synchronize()
+        ms = s_ev.elapsed_time(e_ev) / (replays * n)
+        del g
+        return {"launches_per_graph": n, "ms": round(ms, 5)}
+    except Exception as exc:  # reported, not fatal
+        return {"error": f"{type(exc).__name__}: {exc}"[:200]}
+
+
 def graph_steps(fa, torch, step, sets, flops, n=100, replays=5):
     """The benchmark step captured n times into one CUDA graph (cycling
     through the same rotating input sets) and replayed: device time per step
@@ -408,13 +449,25 @@ def forward_workloads(fa, torch, tflops_peak, peak_src):
         e_ev.record()
         torch.cuda.synchronize()
         ms = s_ev.elapsed_time(e_ev) / reps
+
+        def launch(i, sets=sets, w=w, R=R):
+            t = sets[i % R]
+            fa.fa_forward(t["q"], t["k"], t["v"], t["o"], t["lse"], w.scale, w.causal)
+
         tf = w.fwd_flops() / (ms * 1e-3) / 1e12
-        out.append({"workload": w.describe(), "ms": round(ms, 4), "tflops": round(tf, 1),
-                    "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst",
-                    "input_sets": R})
+        line = {"workload": w.describe(), "ms": round(ms, 4), "tflops": round(tf, 1),
+                "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst",
+                "input_sets": R, "per_launch_ms": per_launch_ms(torch, launch)}
+        if name == GRAPH_FWD_WORKLOAD:
+            line["graph"] = graph_launches(torch, launch)
+        out.append(line)
         del sets, inp
         torch.cuda.empty_cache()
     return out
+
+
+# The forward workload also timed as a 100-launch CUDA graph.
+GRAPH_FWD_WORKLOAD = "causal_n4096_d64"
 
 
 # Backward beside the benchmark step: the d = 128 and d = 96 kernel on the
@@ -453,8 +506,10 @@ def backward_workloads(fa, torch, tflops_peak, peak_src):
         torch.cuda.synchronize()
         ms = s_ev.elapsed_time(e_ev) / reps
         tf = 10.0 * B * Hq * N * N * d / 2 / (ms * 1e-3) / 1e12
+        pl = per_launch_ms(torch, lambda i: call(q, k, v, o, lse, do, dq, dk, dv, scale, True))
         out.append({"workload": name, "ms": round(ms, 4), "tflops": round(tf, 1),
-                    "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst"})
+                    "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst",
+                    "per_launch_ms": pl})
         del q, k, v, do, o, lse, dq, dk, dv
         torch.cuda.empty_cache()
     return out
@@ -484,10 +539,11 @@ def forward_fp8_workload(fa, torch, tflops_peak, peak_src):
     ms = s_ev.elapsed_time(e_ev) / reps
     tf = w.fwd_flops() / (ms * 1e-3) / 1e12
     peak = 2.0 * tflops_peak
+    pl = per_launch_ms(torch, lambda i: fa.fa_forward_fp8(q, k, vt, o, lse, w.scale, w.causal))
     out = {"workload": w.describe().replace("bf16", "e4m3 (O bf16)"), "dtype": "e4m3",
            "ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / peak, 4),
            "peak": f"2 x {peak_src} bf16 burst (nominal fp8/bf16 ratio)",
-           "input_sets": 1}
+           "input_sets": 1, "per_launch_ms": pl}
     del q, k, vt, o, lse
     torch.cuda.empty_cache()
     return out
