@@ -300,8 +300,10 @@ __global__ void __launch_bounds__(384, 1)
       // ------------------------------------------------------------ MMA issuer
       if (elect_one()) {
         constexpr uint32_t id_ss = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-        constexpr uint32_t id_kd = idesc_bf16_f32(128, C::DP, false, true);  // dV, dK
-        constexpr uint32_t id_q = idesc_bf16_f32(128, C::DP, true, true);    // dQ
+        // dV, dK and dQ run at N = D (a multiple of 16): at D = 96 the padded
+        // columns of their accumulators are neither computed nor read.
+        constexpr uint32_t id_kd = idesc_bf16_f32(128, D, false, true);  // dV, dK
+        constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);    // dQ
         bool ok = mbar_wait(bar(C::B_KV), 0, abort_flag, p.err, kErrTimeoutMma);
         for (int s = 0; ok && s < n_steps; ++s) {
           const int qs = s % C::NQ;

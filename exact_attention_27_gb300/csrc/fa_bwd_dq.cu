@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);  // S, dP
-      constexpr uint32_t ID_Q = idesc_bf16_f32(128, C::DP, false, true);  // dQ (B = K MN-major)
+      constexpr uint32_t ID_Q = idesc_bf16_f32(128, D, false, true);  // dQ (B = K MN-major), N = D
       const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t do_desc = smem_desc_sw128(sdO, 16, 1024);
       const uint64_t k_kmaj = smem_desc_sw128(sK, 16, 1024);

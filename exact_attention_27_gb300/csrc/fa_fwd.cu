@@ -75,8 +75,8 @@ constexpr float kRescaleThreshold = 8.0f;
 // Head dimension D in {64, 96, 128}.  Tiles are stored DP = D rounded up to
 // a multiple of 64 columns wide (whole 128-byte swizzle atoms); for D = 96
 // the copies fill columns 96..127 with zeros (they lie outside the tensor),
-// Q K^T runs over the D real columns only, and P V runs at N = DP, whose
-// extra output columns stay zero and are never stored.
+// Q K^T runs over the D real columns only, and P V runs at N = D (a
+// multiple of 16, as the MMA allows), so no O column past D is computed.
 //
 // FP8 = true: Q, K and V^T are e4m3 (one byte per element, D = 128: one
 // 128-byte row per tile row, so SUB = 1), the products run as kind::f8f6f4,
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t ID_S =
           FP8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t ID_O =
-          FP8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, C::DP, false, true);
+          FP8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, false, true);
       const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t k_desc = smem_desc_sw128(sK, 16, 1024);
       // bf16: V is [keys][d], read MN-major; FP8: V^T is [d][keys], read K-major.
