@@ -118,8 +118,7 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float4* __restri
 
 // Head dimension D in {96, 128} (64 has its own kernel).  Tiles are DP = 128
 // columns wide; for D = 96 the copies zero-fill columns 96..127, S^T and dP^T
-// contract over the D real columns, and dV, dK and dQ run at N = DP with
-// zero extra columns that are never stored.
+// contract over the D real columns, and dV, dK and dQ run at N = D.
 template <int D>
 struct BwdCfg {
   static constexpr int DP = (D + 63) / 64 * 64;  // padded head dimension

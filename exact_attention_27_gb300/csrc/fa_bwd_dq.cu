@@ -33,7 +33,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Head dimension D in {64, 96, 128}; tiles are DP = D rounded up to a
 // multiple of 64 columns wide (zero-filled past D), S and dP contract over the
-// D real columns and dQ runs at N = DP.
+// D real columns and dQ runs at N = D.
 template <int D>
 struct DqCfg {
   static constexpr int DP = (D + 63) / 64 * 64;  // padded head dimension
