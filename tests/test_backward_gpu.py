@@ -64,6 +64,15 @@ def test_grouped_query_heads(G, d):
     bwd_vs_oracle(inp, True, 1.0 / math.sqrt(d))
 
 
+@pytest.mark.parametrize("d", [64, 96, 128])
+@pytest.mark.parametrize("N", [200, 513])
+def test_grouped_query_heads_non_causal(d, N):
+    """Non-causal: every key tile sees every query tile of all G heads of its
+    group, so dK and dV sum over the whole group at every key."""
+    inp = make_inputs(2, 8, 2, N, d, seed=700 + N + d, with_grad=True)
+    bwd_vs_oracle(inp, False, 1.0 / math.sqrt(d))
+
+
 @pytest.mark.parametrize("N", [1, 70, 129, 600])
 @pytest.mark.parametrize("causal", [False, True])
 def test_head_dim_96(N, causal):
