@@ -509,7 +509,10 @@ __global__ void __launch_bounds__(448, 1)
       }
       if (!ok) break;
     }
-    if (t == 0) bulk_wait_group0();
+    // Only the staging tile's reads must be over before the epilogue; the
+    // reduces' writes complete on their own, and the dQ finalisation reads
+    // the accumulator only after this grid has completed.
+    if (t == 0) bulk_wait_group_read0();
     __syncwarp();  // lane 0 waited alone; the TMEM loads below are warp-collective
     grid_launch_dependents();  // the dQ finalisation may be scheduled
     // ---- epilogue, once every MMA has completed
