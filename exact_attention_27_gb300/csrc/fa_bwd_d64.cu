@@ -18,13 +18,17 @@
 //    half, each on 32 of its 64 query columns, which halves the dependent
 //    chain each warp runs per half (the work there is latency-bound).
 //  * A third warpgroup copies K and V into TMEM, stages L and D of upcoming
-//    halves into a shared-memory ring, drains each query tile's dQ through a
-//    swizzled staging tile and a TMA reduce-add into the fp32 accumulator,
-//    and writes dK (times scale) and dV at the end.
+//    halves into a shared-memory ring and drains each query tile's dQ
+//    through a swizzled staging tile and a TMA reduce-add into the fp32
+//    accumulator.  At the end the two compute warpgroups write dK (times
+//    scale) and dV, one each, while it drains the last dQ.
+//  * The producer's lane initialises the barriers and issues the K, V and
+//    first Q/dO loads before the CTA barrier, so that their latency overlaps
+//    the tensor-memory allocation.
 //
-// Warps: 0-3 compute (query columns 0-31 of each half), 4-7 compute (columns
-// 32-63), 8-11 L/D staging, dQ drain and epilogue, 12 TMA producer, 13 MMA
-// issuer.  448 threads, 1 CTA per SM.
+// Warps: 0-3 compute (query columns 0-31 of each half) and dK, 4-7 compute
+// (columns 32-63) and dV, 8-11 L/D staging and dQ drain, 12 TMA producer,
+// 13 MMA issuer.  448 threads, 1 CTA per SM.
 //
 // Tensor memory (512 columns):
 //   [  0, 64) dK      [ 64,128) dV      [128,160) K bf16   [160,192) V bf16
@@ -151,7 +155,31 @@ __global__ void __launch_bounds__(448, 1)
   const int n_steps = p.G * per_head;
   const int n_half = 2 * n_steps;
 
-  if (threadIdx.x == 0) {
+  const uint32_t sK = sbase + C::OFF_K;
+  const uint32_t sV = sbase + C::OFF_V;
+  const uint32_t sQ = sbase + C::OFF_Q;
+  const uint32_t sdO = sbase + C::OFF_DO;
+  const uint32_t sDS = sbase + C::OFF_DS;
+  const uint32_t sSTG = sbase + C::OFF_STG;
+
+  // step -> (query head within the group, query tile)
+  auto step_coords = [&](int s, int& bhq, int& it) {
+    const int g = s / per_head;
+    it = i0 + (s - g * per_head);
+    bhq = b * p.Hq + hkv * p.G + g;
+  };
+
+  // The producer's lane initialises the barriers and issues the loads of K,
+  // V and the first Q/dO stages at once, so that their latency overlaps the
+  // tensor-memory allocation and the CTA barrier below.  (K, V, Q and dO are
+  // inputs of the backward, which this grid may read before it waits for
+  // the grid before it.)
+  const int first_loads = min(C::NSQ, n_steps);
+  if (warp == 12 && elect_one()) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
     mbar_init(bar(C::B_KV), 1);
     mbar_init(bar(C::B_KVT), 4);  // one arrival per warp of the drain warpgroup
     for (int s = 0; s < C::NSQ; ++s) {
@@ -174,6 +202,16 @@ __global__ void __launch_bounds__(448, 1)
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
+    mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE);
+    tma_load_3d(sK, &tmK, bar(C::B_KV), 0, jt * C::BK, kvz);
+    tma_load_3d(sV, &tmV, bar(C::B_KV), 0, jt * C::BK, kvz);
+    for (int s = 0; s < first_loads; ++s) {
+      int bhq, it;
+      step_coords(s, bhq, it);
+      mbar_arrive_expect_tx(bar(C::B_QDFULL + s), 2 * C::TILE);
+      tma_load_3d(sQ + s * C::TILE, &tmQ, bar(C::B_QDFULL + s), 0, it * C::BQ, bhq);
+      tma_load_3d(sdO + s * C::TILE, &tmdO, bar(C::B_QDFULL + s), 0, it * C::BQ, bhq);
+    }
   }
   if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -184,32 +222,12 @@ __global__ void __launch_bounds__(448, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const uint32_t sK = sbase + C::OFF_K;
-  const uint32_t sV = sbase + C::OFF_V;
-  const uint32_t sQ = sbase + C::OFF_Q;
-  const uint32_t sdO = sbase + C::OFF_DO;
-  const uint32_t sDS = sbase + C::OFF_DS;
-  const uint32_t sSTG = sbase + C::OFF_STG;
-
-  // step -> (query head within the group, query tile)
-  auto step_coords = [&](int s, int& bhq, int& it) {
-    const int g = s / per_head;
-    it = i0 + (s - g * per_head);
-    bhq = b * p.Hq + hkv * p.G + g;
-  };
-
   if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE);
-      tma_load_3d(sK, &tmK, bar(C::B_KV), 0, jt * C::BK, kvz);
-      tma_load_3d(sV, &tmV, bar(C::B_KV), 0, jt * C::BK, kvz);
-      int issued = 0;
-      for (int s = 0; s < n_steps; ++s) {
+      // K, V and steps 0 .. first_loads - 1 were issued before the CTA barrier.
+      int issued = first_loads;
+      for (int s = first_loads; s < n_steps; ++s) {
         const int st = s % C::NSQ;
         if (s >= C::NSQ && !mbar_wait(bar(C::B_QDEMPTY + st), ((s / C::NSQ) - 1) & 1,
                                       abort_flag, p.err, kErrTimeoutLoad))
@@ -407,8 +425,34 @@ __global__ void __launch_bounds__(448, 1)
       mbar_arrive_warp(bar(C::B_PDS + a));
       mbar_arrive_warp(bar(C::B_LDEMPTY + h % C::NLD));  // this half's L/D are no longer read
     }
+    // ---- epilogue, once every MMA has completed: warpgroup 0 writes dK
+    // (times scale), warpgroup 1 dV, while the drain finishes the last dQ.
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_FINAL), 0, abort_flag, p.err,
+                                                   kErrTimeoutEpilogue));
+    if (ok) {
+      tc_fence_after();
+      const float mul = wg == 0 ? p.scale : 1.0f;
+      __nv_bfloat16* row = (wg == 0 ? p.dk : p.dv) +
+                           (static_cast<size_t>(kvz) * p.N + (key_live ? key : 0)) * 64;
+#pragma unroll
+      for (int q4 = 0; q4 < 2; ++q4) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + (wg == 0 ? C::COL_DK : C::COL_DV) + q4 * 32, r);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          pk[u] = pack_bf16x2(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
+        if (key_live) {
+          uint4* dst = reinterpret_cast<uint4*>(row + q4 * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+    }
   } else if (wg == 2) {
-    // ------------------------------------------------------------ K/V -> TMEM, dQ drain, epilogue
+    // ------------------------------------------------------------ K/V -> TMEM, L/D ring, dQ drain
     const int t = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t wg_phase = 0;
@@ -509,45 +553,12 @@ __global__ void __launch_bounds__(448, 1)
       }
       if (!ok) break;
     }
-    // Only the staging tile's reads must be over before the epilogue; the
-    // reduces' writes complete on their own, and the dQ finalisation reads
-    // the accumulator only after this grid has completed.
+    // Only the staging tile's reads must be over before the CTA's shared
+    // memory is released; the reduces' writes complete on their own, and the
+    // dQ finalisation reads the accumulator only after this grid has completed.
     if (t == 0) bulk_wait_group_read0();
-    __syncwarp();  // lane 0 waited alone; the TMEM loads below are warp-collective
+    __syncwarp();
     grid_launch_dependents();  // the dQ finalisation may be scheduled
-    // ---- epilogue, once every MMA has completed
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_FINAL), 0, abort_flag, p.err,
-                                                   kErrTimeoutEpilogue));
-    if (ok) {
-      tc_fence_after();
-      const int key = jt * C::BK + t;
-      const bool live = key < p.N;
-      __nv_bfloat16* dk_row = p.dk + (static_cast<size_t>(kvz) * p.N + (live ? key : 0)) * 64;
-      __nv_bfloat16* dv_row = p.dv + (static_cast<size_t>(kvz) * p.N + (live ? key : 0)) * 64;
-#pragma unroll
-      for (int q4 = 0; q4 < 2; ++q4) {
-        uint32_t rk[32], rv[32];
-        tmem_ld32(tmem + lane_off + C::COL_DK + q4 * 32, rk);
-        tmem_ld32(tmem + lane_off + C::COL_DV + q4 * 32, rv);
-        tmem_wait_ld();
-        uint32_t pkk[16], pkv[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          pkk[u] = pack_bf16x2(__uint_as_float(rk[2 * u]) * p.scale,
-                               __uint_as_float(rk[2 * u + 1]) * p.scale);
-          pkv[u] = pack_bf16x2(__uint_as_float(rv[2 * u]), __uint_as_float(rv[2 * u + 1]));
-        }
-        if (live) {
-          uint4* dst_k = reinterpret_cast<uint4*>(dk_row + q4 * 32);
-          uint4* dst_v = reinterpret_cast<uint4*>(dv_row + q4 * 32);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            dst_k[u] = make_uint4(pkk[4 * u], pkk[4 * u + 1], pkk[4 * u + 2], pkk[4 * u + 3]);
-            dst_v[u] = make_uint4(pkv[4 * u], pkv[4 * u + 1], pkv[4 * u + 2], pkv[4 * u + 3]);
-          }
-        }
-      }
-    }
   }
 
   // Every warp reconverges first: in the TMA and MMA warps only one lane did
