@@ -187,6 +187,29 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// This thread's row of an fp32 TMEM accumulator (D columns from `taddr`)
+// times `mul`, as bf16 into `row` (skipped for rows past N).  Warp-collective.
+template <int D>
+__device__ __forceinline__ void write_rows(uint32_t taddr, __nv_bfloat16* row, float mul,
+                                           bool live) {
+#pragma unroll
+  for (int q4 = 0; q4 < D / 32; ++q4) {
+    uint32_t r[32];
+    tmem_ld32(taddr + q4 * 32, r);
+    tmem_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      pk[u] = pack_bf16x2(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
+    if (live) {
+      uint4* dst = reinterpret_cast<uint4*>(row + q4 * 32);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+    }
+  }
+}
+
 // DQ = false builds the dK/dV-only kernel of the deterministic backward.
 template <int D, bool CAUSAL, bool DQ>
 __global__ void __launch_bounds__(384, 1)
@@ -213,7 +236,23 @@ __global__ void __launch_bounds__(384, 1)
   const int per_head = p.n_qtiles - i0;
   const int n_steps = p.G * per_head;
 
-  if (threadIdx.x == 0) {
+  const uint32_t sK = sbase + C::OFF_K;
+  const uint32_t sV = sbase + C::OFF_V;
+  const uint32_t sQ = sbase + C::OFF_Q;
+  const uint32_t sdO = sbase + C::OFF_DO;
+  const uint32_t sDS = sbase + C::OFF_DS;
+  const uint32_t sSTG = sbase + C::OFF_STG;
+
+  // The producer's lane initialises the barriers and issues the loads of K,
+  // V and step 0's Q and dO at once, so that their latency overlaps the
+  // tensor-memory allocation and the CTA barrier below.  (K, V, Q and dO are
+  // inputs of the backward, which this grid may read before it waits for
+  // the grid before it.)
+  if (warp == 8 && elect_one()) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
     mbar_init(bar(C::B_KV), 1);
     for (int s = 0; s < C::NQ; ++s) {
       mbar_init(bar(C::B_QFULL + s), 1);
@@ -230,6 +269,22 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
+    mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE);
+#pragma unroll
+    for (int s = 0; s < C::SUB; ++s) {
+      tma_load_3d(sK + s * C::SUB_BYTES, &tmK, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
+      tma_load_3d(sV + s * C::SUB_BYTES, &tmV, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
+    }
+    if (n_steps > 0) {  // step 0: query head 0 of the group, query tile i0
+      const int bhq = b * p.Hq + hkv * p.G;
+      mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE);
+      mbar_arrive_expect_tx(bar(C::B_DOFULL), C::TILE);
+#pragma unroll
+      for (int s = 0; s < C::SUB; ++s) {
+        tma_load_3d(sQ + s * C::SUB_BYTES, &tmQ, bar(C::B_QFULL), 64 * s, i0 * C::BQ, bhq);
+        tma_load_3d(sdO + s * C::SUB_BYTES, &tmdO, bar(C::B_DOFULL), 64 * s, i0 * C::BQ, bhq);
+      }
+    }
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -240,32 +295,16 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const uint32_t sK = sbase + C::OFF_K;
-  const uint32_t sV = sbase + C::OFF_V;
-  const uint32_t sQ = sbase + C::OFF_Q;
-  const uint32_t sdO = sbase + C::OFF_DO;
-  const uint32_t sDS = sbase + C::OFF_DS;
-  const uint32_t sSTG = sbase + C::OFF_STG;
-
   if (warp >= 8) {
     reg_decrease<152>();
     if (warp == 8) {
       // ------------------------------------------------------------ TMA producer
       if (elect_one()) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-        tma_prefetch_desc(&tmdO);
-        mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE);
-  #pragma unroll
-        for (int s = 0; s < C::SUB; ++s) {
-          tma_load_3d(sK + s * C::SUB_BYTES, &tmK, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
-          tma_load_3d(sV + s * C::SUB_BYTES, &tmV, bar(C::B_KV), 64 * s, jt * C::BK, kvz);
-        }
         // Q of step s into stage s % NQ, dO into its single stage; each waits
-        // for the step that last used its buffer.
-        int q_issued = 0, do_issued = 0;
-        for (int st_i = 0; st_i < n_steps; ++st_i) {
+        // for the step that last used its buffer.  K, V and step 0 were
+        // issued before the CTA barrier.
+        int q_issued = n_steps > 0 ? 1 : 0, do_issued = q_issued;
+        for (int st_i = 1; st_i < n_steps; ++st_i) {
           const int g = st_i / per_head;
           const int it = i0 + (st_i - g * per_head);
           const int bhq = b * p.Hq + hkv * p.G + g;
@@ -480,32 +519,11 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQFULL), (n_steps - 1) & 1, abort_flag,
                                              p.err, kErrTimeoutEpilogue));
     if (ok) {
+      // dK (times scale); the drain warpgroup writes dV meanwhile.
       tc_fence_after();
-      __nv_bfloat16* dk_row = p.dk + (static_cast<size_t>(kvz) * p.N + (key_live ? key : 0)) * D;
-      __nv_bfloat16* dv_row = p.dv + (static_cast<size_t>(kvz) * p.N + (key_live ? key : 0)) * D;
-#pragma unroll
-      for (int q4 = 0; q4 < D / 32; ++q4) {
-        uint32_t rk[32], rv[32];
-        tmem_ld32(tmem + lane_off + C::COL_DK + q4 * 32, rk);
-        tmem_ld32(tmem + lane_off + C::COL_DV + q4 * 32, rv);
-        tmem_wait_ld();
-        uint32_t pkk[16], pkv[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          pkk[u] = pack_bf16x2(__uint_as_float(rk[2 * u]) * p.scale,
-                               __uint_as_float(rk[2 * u + 1]) * p.scale);
-          pkv[u] = pack_bf16x2(__uint_as_float(rv[2 * u]), __uint_as_float(rv[2 * u + 1]));
-        }
-        if (key_live) {
-          uint4* dst_k = reinterpret_cast<uint4*>(dk_row + q4 * 32);
-          uint4* dst_v = reinterpret_cast<uint4*>(dv_row + q4 * 32);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            dst_k[u] = make_uint4(pkk[4 * u], pkk[4 * u + 1], pkk[4 * u + 2], pkk[4 * u + 3]);
-            dst_v[u] = make_uint4(pkv[4 * u], pkv[4 * u + 1], pkv[4 * u + 2], pkv[4 * u + 3]);
-          }
-        }
-      }
+      write_rows<D>(tmem + lane_off + C::COL_DK,
+                    p.dk + (static_cast<size_t>(kvz) * p.N + (key_live ? key : 0)) * D, p.scale,
+                    key_live);
     }
   } else {
     reg_decrease<152>();
@@ -561,9 +579,19 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
     }
-    // Only the staging tile's reads must be over before the epilogue; the
-    // reduces' writes complete on their own, and the dQ finalisation reads
-    // the accumulator only after this grid has completed.
+    // dV, once the last step's products have completed (its dQ commit, which
+    // the loop waited for, covers them); the key-row warpgroup writes dK.
+    if (ok && n_steps > 0) {
+      tc_fence_after();
+      const int vkey = jt * C::BK + t;  // lane t of this warp's quarter is key row t
+      const bool vlive = vkey < p.N;
+      write_rows<D>(tmem + lane_off + C::COL_DV,
+                    p.dv + (static_cast<size_t>(kvz) * p.N + (vlive ? vkey : 0)) * D, 1.0f,
+                    vlive);
+    }
+    // Only the staging tile's reads must be over before the CTA's shared
+    // memory is released; the reduces' writes complete on their own, and the
+    // dQ finalisation reads the accumulator only after this grid has completed.
     if (t == 0) bulk_wait_group_read0();
     __syncwarp();
     grid_launch_dependents();  // the dQ finalisation may be scheduled
