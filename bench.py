@@ -421,6 +421,70 @@ def run_forward_only(args):
             "tflops": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1)}
 
 
+TILE_SWEEP_SHAPES = (
+    # (B, H_q, H_kv, N): the shapes the per-shape tile choice was fitted on ...
+    [(1, h, h, n) for h in (2, 4, 8, 16, 32, 64) for n in (1024, 2048, 4096, 8192)
+     if h * n <= 64 * 8192]
+    # ... and shapes held out of the fit (other head counts, GQA, other N).
+    + [(b, h, g, n) for (b, h, g) in ((1, 12, 12), (1, 24, 24), (1, 48, 48), (2, 20, 20),
+                                       (1, 32, 8), (1, 40, 5)) for n in (1536, 3072, 6144)])
+
+
+def run_tile_rows_sweep(args):
+    """fa_forward at 128 and 256 query rows per CTA and at the per-shape
+    choice, on every shape of TILE_SWEEP_SHAPES, d = 64 and 128, causal and
+    not: one JSON line per shape, then the time the choice lost against the
+    faster size, summed over the shapes.  Back-to-back launches (10 timed
+    after 3 warm-up) on the same inputs, timed with CUDA events."""
+    import torch
+    import exact_attention_27_gb300 as fa
+    from exact_attention_27_gb300 import _build
+    _build.build()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def timed(f, n=10):
+        for _ in range(3):
+            f()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(n):
+            f()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / n
+
+    lost, n_shapes = 0.0, 0
+    try:
+        for d in (64, 128):
+            for causal in (True, False):
+                for B, Hq, Hkv, N in TILE_SWEEP_SHAPES:
+                    inp = make_inputs(B, Hq, Hkv, N, d, seed=1)
+                    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+                    o = torch.empty_like(q)
+                    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+                    ms = {}
+                    for rows in (128, 256, 0):
+                        fa.fa_set_forward_tile_rows(rows)
+                        ms[rows] = timed(lambda: fa.fa_forward(q, k, v, o, lse, d ** -0.5, causal))
+                    fa.fa_set_forward_tile_rows(0)
+                    pick = fa.fa_forward_tile_rows_for(B, Hq, Hkv, N, N, d, causal, 0, sms)
+                    best = min(ms[128], ms[256])
+                    lost += ms[pick] / best - 1.0
+                    n_shapes += 1
+                    print(json.dumps({"d": d, "causal": causal, "B": B, "H_q": Hq, "H_kv": Hkv,
+                                      "N": N, "ms_128": round(ms[128], 4),
+                                      "ms_256": round(ms[256], 4), "ms_chosen": round(ms[0], 4),
+                                      "chosen": pick}), flush=True)
+                    del q, k, v, o, lse, inp
+        if fa.fa_last_device_error() != 0:
+            raise RuntimeError("device error")
+    finally:
+        fa.fa_set_forward_tile_rows(0)
+    return {"sweep": "forward tile rows", "shapes": n_shapes, "sms": sms,
+            "summed_loss_vs_faster": round(lost, 3)}
+
+
 def forward_workloads(fa, torch, tflops_peak, peak_src):
     """Forward-only throughput on the larger workloads: back-to-back launches,
     cycling through enough input sets that each launch's inputs come from HBM."""
@@ -789,6 +853,8 @@ def main():
                     help="run fa_forward alone on one workload (for kernel profiles)")
     ap.add_argument("--backward-only", choices=sorted(BWD_NAMES), default=None,
                     help="run fa_backward alone on one backward workload (for kernel profiles)")
+    ap.add_argument("--sweep-tile-rows", action="store_true",
+                    help="time both forward tile sizes and the per-shape choice on a shape grid")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -801,6 +867,9 @@ def main():
         return
     if args.backward_only:
         print(json.dumps(run_backward_only(args)), flush=True)
+        return
+    if args.sweep_tile_rows:
+        print(json.dumps(run_tile_rows_sweep(args)), flush=True)
         return
     if args.impl == "reference":
         if rank == 0:

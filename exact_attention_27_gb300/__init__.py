@@ -18,7 +18,7 @@ import math
 from ._lib import FaError, library, status_string  # noqa: F401
 
 __all__ = [
-    "FaError", "fa_forward", "fa_forward_ex", "fa_forward_fp8", "fa_set_forward_tile_rows",
+    "FaError", "fa_forward", "fa_forward_ex", "fa_forward_fp8", "fa_set_forward_tile_rows", "fa_forward_tile_rows_for",
     "fa_backward", "fa_backward_deterministic", "fa_backward_preprocess", "fa_status_string",
     "fa_last_device_error", "fa_selftest_wait_timeout", "fa_set_backward_events", "attention_forward", "attention_backward",
     "library",
@@ -126,6 +126,13 @@ def fa_forward_fp8(q, k, v_t, o, lse, scale, causal, q_descale=1.0, k_descale=1.
 def fa_set_forward_tile_rows(rows):
     """fa_set_forward_tile_rows of include/fa.h: 0 (per shape), 128 or 256."""
     _check(library().fa_set_forward_tile_rows(int(rows)), "fa_set_forward_tile_rows")
+
+
+def fa_forward_tile_rows_for(B, H_q, H_kv, N_q, N_kv, d, causal, q_offset, sms):
+    """fa_forward_tile_rows_for of include/fa.h: 128 or 256, 0 for invalid sizes."""
+    return int(library().fa_forward_tile_rows_for(int(B), int(H_q), int(H_kv), int(N_q),
+                                                  int(N_kv), int(d), int(bool(causal)),
+                                                  int(q_offset), int(sms)))
 
 
 def fa_backward(q, k, v, o, lse, do, dq, dk, dv, scale, causal, stream=None):

@@ -330,6 +330,16 @@ fa_status fa_set_forward_tile_rows(int rows) {
   return FA_OK;
 }
 
+int fa_forward_tile_rows_for(int B, int H_q, int H_kv, int N_q, int N_kv, int d, int causal,
+                             int q_offset, int sms) {
+  if (validate(B, H_q, H_kv, N_q, d, 1.0f, causal) != FA_OK) return 0;
+  if (N_kv < 1 || q_offset < 0 || sms < 1) return 0;
+  fa::AttnShape s{B, H_q, H_kv, N_q, d, 1.0f, causal};
+  s.Nk = N_kv;
+  s.q_offset = q_offset;
+  return fa::forward_rows_for(s, sms);
+}
+
 void fa_set_backward_events(cudaEvent_t before, cudaEvent_t after) {
   g_bwd_before = before;
   g_bwd_after = after;

@@ -60,7 +60,14 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <array>
 #include <atomic>
+#include <functional>
+#include <map>
+#include <mutex>
+#include <queue>
+#include <vector>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -652,13 +659,86 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 std::atomic<int> g_rows_per_cta{0};
 
 // The per-shape choice between one and two query tiles per CTA.  Two tiles
-// per CTA share each K/V tile between two softmax warpgroups; one tile per
-// CTA makes twice as many CTAs, which wins while the two-tile grid would
-// leave SMs idle or load them unevenly.  Measured on GB300 (152 SMs; d = 64
-// and 128, causal and not, B*H from 2 to 64, N from 1024 to 8192): one tile
-// per CTA is 1.1-1.9x faster while the two-tile grid has fewer CTAs than
-// SMs under the causal mask (fewer than half as many without it), and
-// 0.75-0.95x as fast beyond.
+// per CTA share each K/V tile between two softmax warpgroups and do more
+// work per tile step; one tile per CTA makes twice as many, shorter CTAs,
+// which wins while the two-tile grid would leave SMs idle or end on a short
+// last wave.  Both kernels hold all 512 tensor-memory columns, so an SM runs
+// one CTA at a time, and the choice is made by estimating each grid's finish
+// time: the CTAs, in launch order, each start on the SM that frees first,
+// and a CTA costs its per-CTA overhead plus its key-tile steps.  The costs,
+// in units of one 128 x 128 key-tile step of the two-tile CTA, were fitted
+// on GB300 (152 SMs; d = 64 and 128, causal and not, B*H from 2 to 64,
+// N from 1024 to 8192):
+//   d = 64:  two-tile CTA 1 + steps,  one-tile CTA 6 + 1.4 x steps;
+//   d = 128: two-tile CTA 1 + steps,  one-tile CTA 3 + 1.0 x steps.
+// Past 16 two-tile waves the last wave no longer matters and the two-tile
+// CTA's cheaper steps win.
+std::mutex g_rows_mu;
+std::map<std::array<long long, 8>, int> g_rows_cache;
+
+double list_schedule_finish(int sms, long long n_heads, long long heads_per_group,
+                            long long units, bool causal, const std::function<double(long long)>& cost) {
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int i = 0; i < sms; ++i) free_at.push(0.0);
+  double finish = 0.0;
+  for (long long g0 = 0; g0 < n_heads; g0 += heads_per_group) {
+    const long long in_grp = std::min(heads_per_group, n_heads - g0);
+    for (long long i = 0; i < units; ++i) {
+      const double c = cost(causal ? units - 1 - i : i);
+      for (long long h = 0; h < in_grp; ++h) {
+        const double t = free_at.top() + c;
+        free_at.pop();
+        free_at.push(t);
+        finish = std::max(finish, t);
+      }
+    }
+  }
+  return finish;
+}
+
+}  // namespace
+
+int forward_rows_for(const AttnShape& s, int sms) {
+  if (s.d == 256) return 128;
+  if (s.d != 64 && s.d != 128) return 256;
+  const long long n_qtiles = (static_cast<long long>(s.N) + 127) / 128;
+  const long long n_ktiles = (static_cast<long long>(s.keys()) + 127) / 128;
+  const long long n_pairs = (n_qtiles + 1) / 2;
+  const long long n_heads = static_cast<long long>(s.B) * s.Hq;
+  if (n_heads * n_pairs > 16LL * sms) return 256;
+  const std::array<long long, 8> key{n_heads, s.Hq / s.Hkv, s.N, s.keys(), s.q_offset, s.d,
+                                     s.causal ? 1 : 0, sms};
+  {
+    std::lock_guard<std::mutex> lk(g_rows_mu);
+    const auto it = g_rows_cache.find(key);
+    if (it != g_rows_cache.end()) return it->second;
+  }
+  // Launch-order grouping of heads, as both kernels' hosts size it: K/V of
+  // a group within about 48 MiB of L2, whole GQA groups.
+  const double kv_bytes = 2.0 * s.keys() * s.d * 2.0;
+  long long hpg = std::max(1LL, static_cast<long long>(48.0 * 1024 * 1024 / kv_bytes)) *
+                  (s.Hq / s.Hkv);
+  hpg = std::min(hpg, n_heads);
+  // Key tiles visited by query tile qt (the kernels' causal bound).
+  auto tiles = [&](long long qt) -> double {
+    if (qt >= n_qtiles) return 0.0;
+    if (!s.causal) return static_cast<double>(n_ktiles);
+    return static_cast<double>(std::min((s.q_offset + qt * 128 + 127) / 128 + 1, n_ktiles));
+  };
+  const double o1 = s.d == 64 ? 6.0 : 3.0, r1 = s.d == 64 ? 1.4 : 1.0, o2 = 1.0;
+  const double pair = list_schedule_finish(sms, n_heads, hpg, n_pairs, s.causal != 0,
+                                           [&](long long u) { return o2 + tiles(2 * u) + tiles(2 * u + 1); });
+  const double one = list_schedule_finish(sms, n_heads, hpg, n_qtiles, s.causal != 0,
+                                          [&](long long u) { return o1 + r1 * tiles(u); });
+  const int rows = one < pair ? 128 : 256;
+  std::lock_guard<std::mutex> lk(g_rows_mu);
+  if (g_rows_cache.size() > 1024) g_rows_cache.clear();
+  g_rows_cache.emplace(key, rows);
+  return rows;
+}
+
+namespace {
+
 bool use_one_tile_per_cta(const AttnShape& s) {
   const int forced = g_rows_per_cta.load(std::memory_order_relaxed);
   if (forced == 128) return true;
@@ -670,9 +750,7 @@ bool use_one_tile_per_cta(const AttnShape& s) {
       return 148;
     return n;
   }();
-  const long long qtiles = (static_cast<long long>(s.N) + 127) / 128;
-  const long long pair_ctas = static_cast<long long>(s.B) * s.Hq * ((qtiles + 1) / 2);
-  return pair_ctas * (s.causal ? 1 : 2) < sms;
+  return forward_rows_for(s, sms) == 128;
 }
 
 }  // namespace

@@ -57,6 +57,9 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
 
 // Query rows per CTA for the forward: 0 = chosen per shape, 128 or 256.
 void set_forward_rows_per_cta(int rows);
+// Query rows per CTA (128 or 256) that the bf16 forward chooses for shape s
+// on a GPU with `sms` multiprocessors when no setting forces one; host only.
+int forward_rows_for(const AttnShape& s, int sms);
 int forward_rows_per_cta();
 
 // Backward pass kernels (see fa_bwd.cu).

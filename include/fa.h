@@ -124,8 +124,7 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o,
  * non spreca memoria", section "L'idea: lavorare a tessere", chosen per
  * problem size as the autotuning row of "Flash Attention ... NVIDIA CUDA
  * Tile", section "Resumen: La pila de optimización", does per sequence length:
- *   0    chosen per shape (the default): 256 unless that grid would leave
- *        the GPU's SMs short of work, then 128;
+ *   0    chosen per shape (the default), as fa_forward_tile_rows_for says;
  *   128  one 128-row query tile per CTA;
  *   256  two 128-row query tiles per CTA sharing each K/V tile.
  * Both give the same results up to rounding order.  d = 96 always uses 256,
@@ -133,6 +132,21 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o,
  * other value.
  */
 fa_status fa_set_forward_tile_rows(int rows);
+
+/*
+ * The query rows per CTA (128 or 256) that fa_forward / fa_forward_ex choose
+ * when fa_set_forward_tile_rows is 0, for a problem of those sizes (the
+ * arguments of fa_forward_ex) on a GPU with `sms` multiprocessors.  Each
+ * grid's finish time is estimated by list scheduling: its CTAs, in launch
+ * order, each start on the multiprocessor that frees first, one CTA per
+ * multiprocessor at a time, and cost a per-CTA overhead plus their key-tile
+ * steps at costs fitted on GB300; the grid that finishes first is chosen
+ * (d = 96 always 256, d = 256 always 128).  Pure host computation: needs no
+ * GPU, enqueues nothing.  Returns 0 for arguments fa_forward_ex would reject
+ * (and for sms < 1).
+ */
+int fa_forward_tile_rows_for(int B, int H_q, int H_kv, int N_q, int N_kv, int d, int causal,
+                             int q_offset, int sms);
 
 /*
  * Backward pass.  Source: "L'attention fusionnee", section "La passe
