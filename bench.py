@@ -434,25 +434,20 @@ def run_tile_rows_sweep(args):
     """fa_forward at 128 and 256 query rows per CTA and at the per-shape
     choice, on every shape of TILE_SWEEP_SHAPES, d = 64 and 128, causal and
     not: one JSON line per shape, then the time the choice lost against the
-    faster size, summed over the shapes.  Back-to-back launches (10 timed
-    after 3 warm-up) on the same inputs, timed with CUDA events."""
+    faster size, summed over the shapes.  Each size runs as 20 launches
+    captured in one CUDA graph and replayed 5 times, timed with CUDA events,
+    so that small shapes measure the kernels rather than the host calls."""
     import torch
     import exact_attention_27_gb300 as fa
     from exact_attention_27_gb300 import _build
     _build.build()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
 
-    def timed(f, n=10):
-        for _ in range(3):
-            f()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        s.record()
-        for _ in range(n):
-            f()
-        e.record()
-        torch.cuda.synchronize()
-        return s.elapsed_time(e) / n
+    def timed(f):
+        r = graph_launches(torch, lambda i: f(), n=20, replays=5)
+        if "ms" not in r:
+            raise RuntimeError(r["error"])
+        return r["ms"]
 
     lost, n_shapes = 0.0, 0
     try:

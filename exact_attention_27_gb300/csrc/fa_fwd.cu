@@ -667,9 +667,9 @@ std::atomic<int> g_rows_per_cta{0};
 // time: the CTAs, in launch order, each start on the SM that frees first,
 // and a CTA costs its per-CTA overhead plus its key-tile steps.  The costs,
 // in units of one 128 x 128 key-tile step of the two-tile CTA, were fitted
-// on GB300 (152 SMs; d = 64 and 128, causal and not, B*H from 2 to 64,
-// N from 1024 to 8192):
-//   d = 64:  two-tile CTA 1 + steps,  one-tile CTA 6 + 1.4 x steps;
+// on GB300 to kernel times from CUDA-graph replay (152 SMs; d = 64 and
+// 128, causal and not, B*H from 2 to 64, N from 1024 to 8192):
+//   d = 64:  two-tile CTA steps,      one-tile CTA 1 + 1.35 x steps;
 //   d = 128: two-tile CTA 1 + steps,  one-tile CTA 3 + 1.0 x steps.
 // Past 16 two-tile waves the last wave no longer matters and the two-tile
 // CTA's cheaper steps win.
@@ -725,7 +725,7 @@ int forward_rows_for(const AttnShape& s, int sms) {
     if (!s.causal) return static_cast<double>(n_ktiles);
     return static_cast<double>(std::min((s.q_offset + qt * 128 + 127) / 128 + 1, n_ktiles));
   };
-  const double o1 = s.d == 64 ? 6.0 : 3.0, r1 = s.d == 64 ? 1.4 : 1.0, o2 = 1.0;
+  const double o1 = s.d == 64 ? 1.0 : 3.0, r1 = s.d == 64 ? 1.35 : 1.0, o2 = s.d == 64 ? 0.0 : 1.0;
   const double pair = list_schedule_finish(sms, n_heads, hpg, n_pairs, s.causal != 0,
                                            [&](long long u) { return o2 + tiles(2 * u) + tiles(2 * u + 1); });
   const double one = list_schedule_finish(sms, n_heads, hpg, n_qtiles, s.causal != 0,
