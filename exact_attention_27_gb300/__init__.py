@@ -31,10 +31,34 @@ FA_ERR_CUDA = 3
 FA_ERR_DEVICE_TIMEOUT = 4
 
 
+# torch is imported on first use; the current-stream handle is read with
+# torch's raw getter where it has one (a Stream object per call costs
+# microseconds of host time).
+_torch = None
+_BF16 = _F32 = None
+_current_stream = None
+
+
+def _torch_mod():
+    global _torch, _BF16, _F32, _current_stream
+    if _torch is None:
+        import torch
+        _BF16, _F32 = torch.bfloat16, torch.float32
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        dev = getattr(torch._C, "_cuda_getDevice", None)
+        if raw is not None and dev is not None:
+            _current_stream = lambda: raw(dev())
+        else:
+            _current_stream = lambda: torch.cuda.current_stream().cuda_stream
+        _torch = torch
+    return _torch
+
+
 def _stream(stream):
     if stream is None:
-        import torch
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        if _torch is None:
+            _torch_mod()
+        return ctypes.c_void_p(_current_stream())
     if isinstance(stream, int):
         return ctypes.c_void_p(stream)
     return ctypes.c_void_p(stream.cuda_stream)
@@ -46,18 +70,20 @@ def _check(status, what):
 
 
 def _bf16_cuda(name, t, shape=None):
-    import torch
-    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+    if _torch is None:
+        _torch_mod()
+    if t.dtype is not _BF16 or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if shape is not None and t.shape != shape:
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
 def _f32_cuda(name, t, shape):
-    import torch
-    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+    if _torch is None:
+        _torch_mod()
+    if t.dtype is not _F32 or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 

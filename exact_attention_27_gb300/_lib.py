@@ -65,6 +65,8 @@ def _declare(lib):
 def library():
     """The loaded CUDA library; raises if it was not built or cannot load."""
     global _lib, _load_error
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None and _load_error is None:
             if not os.path.exists(LIB_PATH):

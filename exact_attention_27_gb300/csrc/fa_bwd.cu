@@ -644,8 +644,7 @@ cudaError_t launch_bwd_t(const BwdMaps& m, const float* lse, const float* Dv, vo
                          const AttnShape& s, uint32_t* err, cudaStream_t stream) {
   using C = BwdCfg<D>;
   auto kern = fa_bwd_kernel<D, CAUSAL, DQ>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  cudaError_t e = set_smem_limit_once<fa_bwd_kernel<D, CAUSAL, DQ>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   BwdParams p;
   p.lse = lse;

@@ -578,8 +578,7 @@ cudaError_t launch_t(const BwdMaps& m, const float* lse, const float* Dv, void* 
                      const AttnShape& s, uint32_t* err, cudaStream_t stream) {
   using C = Cfg64;
   auto kern = fa_bwd64_kernel<CAUSAL, DQ>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  cudaError_t e = set_smem_limit_once<fa_bwd64_kernel<CAUSAL, DQ>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   Params64 p;
   p.lse = lse;

@@ -325,8 +325,7 @@ cudaError_t launch_dq_t(const BwdMaps& m, const float* lse, const float* Dv, voi
                         const AttnShape& s, uint32_t* err, cudaStream_t stream) {
   using C = DqCfg<D>;
   auto kern = fa_bwd_dq_kernel<D, CAUSAL>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  cudaError_t e = set_smem_limit_once<fa_bwd_dq_kernel<D, CAUSAL>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   DqParams p;
   p.lse = lse;

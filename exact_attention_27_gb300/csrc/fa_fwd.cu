@@ -619,8 +619,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                          cudaStream_t stream, float o_scale = 1.0f) {
   using C = FwdCfg<D, FP8>;
   auto kern = fa_fwd_kernel<D, CAUSAL, FP8>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  cudaError_t e = set_smem_limit_once<fa_fwd_kernel<D, CAUSAL, FP8>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   FwdParams p;
   p.o = static_cast<__nv_bfloat16*>(o);

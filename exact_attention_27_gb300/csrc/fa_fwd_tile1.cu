@@ -429,8 +429,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                      float* lse, const AttnShape& s, uint32_t* err, cudaStream_t stream) {
   using C = Cfg1<D>;
   auto kern = fa_fwd1_kernel<D, CAUSAL>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  cudaError_t e = set_smem_limit_once<fa_fwd1_kernel<D, CAUSAL>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   Fwd1Params p;
   p.o = static_cast<__nv_bfloat16*>(o);

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include <cstdint>
 #include <utility>
 
@@ -53,6 +55,24 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Raises kernel Kern's dynamic shared-memory limit to `bytes` once per
+// device instead of at every launch (the attribute call costs microseconds
+// of host time; the setting belongs to the device's context, so each device
+// ordinal below 64 is remembered separately and higher ordinals set it each
+// time).
+template <auto Kern>
+cudaError_t set_smem_limit_once(int bytes) {
+  static std::atomic<unsigned long long> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 // Query rows per CTA for the forward: 0 = chosen per shape, 128 or 256.
