@@ -432,7 +432,7 @@ TILE_SWEEP_SHAPES = (
 
 def run_tile_rows_sweep(args):
     """fa_forward at 128 and 256 query rows per CTA and at the per-shape
-    choice, on every shape of TILE_SWEEP_SHAPES, d = 64 and 128, causal and
+    choice, on every shape of TILE_SWEEP_SHAPES, d = 64, 96 and 128, causal and
     not: one JSON line per shape, then the time the choice lost against the
     faster size, summed over the shapes.  Each size runs as 20 launches
     captured in one CUDA graph and replayed 5 times, timed with CUDA events,
@@ -451,7 +451,7 @@ def run_tile_rows_sweep(args):
 
     lost, n_shapes = 0.0, 0
     try:
-        for d in (64, 128):
+        for d in (64, 96, 128):
             for causal in (True, False):
                 for B, Hq, Hkv, N in TILE_SWEEP_SHAPES:
                     inp = make_inputs(B, Hq, Hkv, N, d, seed=1)

@@ -666,9 +666,10 @@ std::atomic<int> g_rows_per_cta{0};
 // time: the CTAs, in launch order, each start on the SM that frees first,
 // and a CTA costs its per-CTA overhead plus its key-tile steps.  The costs,
 // in units of one 128 x 128 key-tile step of the two-tile CTA, were fitted
-// on GB300 to kernel times from CUDA-graph replay (152 SMs; d = 64 and
-// 128, causal and not, B*H from 2 to 64, N from 1024 to 8192):
+// on GB300 to kernel times from CUDA-graph replay (152 SMs; d = 64, 96
+// and 128, causal and not, B*H from 2 to 64, N from 1024 to 8192):
 //   d = 64:  two-tile CTA steps,      one-tile CTA 1 + 1.35 x steps;
+//   d = 96:  two-tile CTA 1 + steps,  one-tile CTA 2.5 + 1.05 x steps;
 //   d = 128: two-tile CTA 1 + steps,  one-tile CTA 3 + 1.0 x steps.
 // Past 16 two-tile waves the last wave no longer matters and the two-tile
 // CTA's cheaper steps win.
@@ -699,7 +700,7 @@ double list_schedule_finish(int sms, long long n_heads, long long heads_per_grou
 
 int forward_rows_for(const AttnShape& s, int sms) {
   if (s.d == 256) return 128;
-  if (s.d != 64 && s.d != 128) return 256;
+  if (s.d != 64 && s.d != 96 && s.d != 128) return 256;
   const long long n_qtiles = (static_cast<long long>(s.N) + 127) / 128;
   const long long n_ktiles = (static_cast<long long>(s.keys()) + 127) / 128;
   const long long n_pairs = (n_qtiles + 1) / 2;
@@ -724,7 +725,11 @@ int forward_rows_for(const AttnShape& s, int sms) {
     if (!s.causal) return static_cast<double>(n_ktiles);
     return static_cast<double>(std::min((s.q_offset + qt * 128 + 127) / 128 + 1, n_ktiles));
   };
-  const double o1 = s.d == 64 ? 1.0 : 3.0, r1 = s.d == 64 ? 1.35 : 1.0, o2 = s.d == 64 ? 0.0 : 1.0;
+  // Per-CTA overhead of the two-tile CTA; overhead and step cost of the
+  // one-tile CTA (the fitted values listed above).
+  const double o2 = s.d == 64 ? 0.0 : 1.0;
+  const double o1 = s.d == 64 ? 1.0 : s.d == 96 ? 2.5 : 3.0;
+  const double r1 = s.d == 64 ? 1.35 : s.d == 96 ? 1.05 : 1.0;
   const double pair = list_schedule_finish(sms, n_heads, hpg, n_pairs, s.causal != 0,
                                            [&](long long u) { return o2 + tiles(2 * u) + tiles(2 * u + 1); });
   const double one = list_schedule_finish(sms, n_heads, hpg, n_qtiles, s.causal != 0,
@@ -761,7 +766,7 @@ cudaError_t launch_forward(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            void* o, float* lse, const AttnShape& s, uint32_t* err,
                            cudaStream_t stream) {
   if (s.d == 256) return launch_forward_tile1(tq, tk, tv, o, lse, s, err, stream);
-  if ((s.d == 64 || s.d == 128) && use_one_tile_per_cta(s))
+  if ((s.d == 64 || s.d == 96 || s.d == 128) && use_one_tile_per_cta(s))
     return launch_forward_tile1(tq, tk, tv, o, lse, s, err, stream);
   if (s.d == 64)
     return s.causal ? launch_fwd_t<64, true>(tq, tk, tv, o, lse, s, err, stream)

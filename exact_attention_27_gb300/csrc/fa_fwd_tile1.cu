@@ -7,8 +7,8 @@
 // two tiles (B_r = 256).  It is the only forward for d = 256 (a 128 x 256
 // bf16 query tile is 64 KB and its fp32 O takes 256 of the 512 TMEM columns,
 // so keys come in tiles of 64 there), and the alternative tile size for
-// d = 64 and 128 (keys in tiles of 128): twice as many CTAs, which covers the
-// SMs better when there are few query tiles.
+// d = 64, 96 and 128 (keys in tiles of 128): twice as many CTAs, which covers
+// the SMs better when there are few query tiles.
 //
 // Pipeline: the S tile of key tile j is computed into tensor-memory buffer
 // j mod 3, so the tensor core computes S_{j+1} and S_{j+2} (and O += P_j V_j)
@@ -29,7 +29,8 @@
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   columns BN*b .. BN*b + BN - 1   S buffer b = 0, 1, 2 (P as packed bf16
 //                                   over its first BN/2 columns)
-//   columns 512 - D .. 511          O accumulator (fp32)
+//   columns 512 - DP .. 512 - DP + D - 1   O accumulator (fp32; DP = D
+//                                   rounded up to a multiple of 64)
 //
 // Every mbarrier wait is bounded (about a second); on expiry the kernel sets
 // an error bit, every role skips its remaining work and the CTA exits.
@@ -50,10 +51,15 @@ constexpr float kRescaleThreshold = 8.0f;
 
 template <int D_>
 struct Cfg1 {
-  static constexpr int D = D_;                   // 64, 128 or 256
+  static constexpr int D = D_;                   // 64, 96, 128 or 256
+  // Tiles are stored DP = D rounded up to whole 128-byte swizzle atoms wide;
+  // at D = 96 the copies fill columns 96..127 with zeros (outside the
+  // tensor), Q K^T runs its 16-column k-steps over the first 96 and
+  // O += P V has N = 96.
+  static constexpr int DP = (D + 63) / 64 * 64;
   static constexpr int BM = 128;                 // query rows per tile (MMA M)
   static constexpr int BN = D == 256 ? 64 : 128; // keys per tile (MMA N of Q K^T)
-  static constexpr int SUB = D / 64;             // 128-byte column blocks per row
+  static constexpr int SUB = DP / 64;            // 128-byte column blocks per row
   static constexpr int Q_BLOCK = BM * 128;       // one 128-row x 64-col block
   static constexpr int KV_BLOCK = BN * 128;      // one BN-row x 64-col block
   static constexpr int Q_TILE = SUB * Q_BLOCK;
@@ -80,8 +86,8 @@ struct Cfg1 {
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int THREADS = 192;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O = 512 - D;   // above the NB S buffers
-  static_assert(NB * BN <= 512 - D, "tensor memory");
+  static constexpr uint32_t COL_O = 512 - DP;  // above the NB S buffers
+  static_assert(NB * BN <= 512 - DP, "tensor memory");
 };
 
 struct Fwd1Params {
@@ -462,7 +468,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 
 }  // namespace
 
-// d in {64, 128, 256}.  K and V maps have boxes of one key tile (64 rows
+// d in {64, 96, 128, 256}.  K and V maps have boxes of one key tile (64 rows
 // for d = 256, else 128) x 64 columns; the query map boxes of 128 x 64.
 cudaError_t launch_forward_tile1(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, void* o, float* lse, const AttnShape& s,
@@ -473,6 +479,9 @@ cudaError_t launch_forward_tile1(const CUtensorMap& tq, const CUtensorMap& tk,
   if (s.d == 128)
     return s.causal ? launch_t<128, true>(tq, tk, tv, o, lse, s, err, stream)
                     : launch_t<128, false>(tq, tk, tv, o, lse, s, err, stream);
+  if (s.d == 96)
+    return s.causal ? launch_t<96, true>(tq, tk, tv, o, lse, s, err, stream)
+                    : launch_t<96, false>(tq, tk, tv, o, lse, s, err, stream);
   if (s.d == 64)
     return s.causal ? launch_t<64, true>(tq, tk, tv, o, lse, s, err, stream)
                     : launch_t<64, false>(tq, tk, tv, o, lse, s, err, stream);

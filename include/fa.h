@@ -120,16 +120,16 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o,
 
 /*
  * Query rows per CTA of the bf16 forward (fa_forward, fa_forward_ex) at
- * d = 64 and 128 — the B_r of the tiling in "FlashAttention: l'attenzione che
- * non spreca memoria", section "L'idea: lavorare a tessere", chosen per
- * problem size as the autotuning row of "Flash Attention ... NVIDIA CUDA
- * Tile", section "Resumen: La pila de optimización", does per sequence length:
+ * d = 64, 96 and 128 — the B_r of the tiling in "FlashAttention:
+ * l'attenzione che non spreca memoria", section "L'idea: lavorare a
+ * tessere", chosen per problem size as the autotuning row of "Flash
+ * Attention ... NVIDIA CUDA Tile", section "Resumen: La pila de
+ * optimización", does per sequence length:
  *   0    chosen per shape (the default), as fa_forward_tile_rows_for says;
  *   128  one 128-row query tile per CTA;
  *   256  two 128-row query tiles per CTA sharing each K/V tile.
- * Both give the same results up to rounding order.  d = 96 always uses 256,
- * d = 256 always 128.  Process-wide; returns FA_ERR_INVALID_ARGUMENT for any
- * other value.
+ * Both give the same results up to rounding order.  d = 256 always uses
+ * 128.  Process-wide; returns FA_ERR_INVALID_ARGUMENT for any other value.
  */
 fa_status fa_set_forward_tile_rows(int rows);
 
@@ -141,9 +141,9 @@ fa_status fa_set_forward_tile_rows(int rows);
  * order, each start on the multiprocessor that frees first, one CTA per
  * multiprocessor at a time, and cost a per-CTA overhead plus their key-tile
  * steps at costs fitted on GB300; the grid that finishes first is chosen
- * (d = 96 always 256, d = 256 always 128).  Pure host computation: needs no
- * GPU, enqueues nothing.  Returns 0 for arguments fa_forward_ex would reject
- * (and for sms < 1).
+ * (d = 256 always 128).  Pure host computation: needs no GPU, enqueues
+ * nothing.  Returns 0 for arguments fa_forward_ex would reject (and for
+ * sms < 1).
  */
 int fa_forward_tile_rows_for(int B, int H_q, int H_kv, int N_q, int N_kv, int d, int causal,
                              int q_offset, int sms);

@@ -229,20 +229,22 @@ def tile_rows():
 @pytest.mark.parametrize("rows", [128, 256])
 @pytest.mark.parametrize("N,d,causal,Hq,Hkv", [
     (1, 64, True, 2, 1), (129, 64, False, 2, 2), (700, 64, True, 4, 2), (1000, 128, True, 2, 1),
-    (257, 128, False, 4, 4), (2048, 64, True, 2, 2),
+    (257, 128, False, 4, 4), (2048, 64, True, 2, 2), (1, 96, True, 2, 1), (300, 96, False, 4, 2),
+    (1000, 96, True, 2, 2), (2048, 96, False, 2, 1),
 ])
 def test_both_tile_sizes_against_the_oracle(tile_rows, rows, N, d, causal, Hq, Hkv):
-    """One (128 rows) or two (256) query tiles per CTA, forced, at d = 64 and 128."""
+    """One (128 rows) or two (256) query tiles per CTA, forced, at d = 64, 96 and 128."""
     tile_rows(rows)
     inp = make_inputs(1, Hq, Hkv, N, d, seed=N + d + rows)
     forward_vs_oracle(inp, causal, 1.0 / math.sqrt(d))
 
 
 @pytest.mark.parametrize("rows", [128, 256])
-def test_both_tile_sizes_with_query_offset(tile_rows, rows):
+@pytest.mark.parametrize("d", [96, 128])
+def test_both_tile_sizes_with_query_offset(tile_rows, rows, d):
     import exact_attention_27_gb300 as fa
     tile_rows(rows)
-    inp = make_inputs(1, 4, 2, 300, 128, seed=31, Nk=941)
+    inp = make_inputs(1, 4, 2, 300, d, seed=31, Nk=941)
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
     o, lse = fa.attention_forward(q, k, v, causal=True, scale=0.1, q_offset=641)
     torch.cuda.synchronize()
