@@ -10,14 +10,24 @@
 // One CTA owns 128 query rows of one (batch, query head), like the forward:
 //   S_j  = Q K_j^T            tcgen05.mma, operands in shared memory
 //   dP_j = dO V_j^T           tcgen05.mma
-//   P    = exp2(S scale log2e - L log2e), dS = P o (dP - D)   one thread per row
+//   P    = exp2(S scale log2e - L log2e), dS = P o (dP - D)   threads
 //   dQ  += dS K_j             tcgen05.mma, A = dS (bf16) from tensor memory
 // and at the end dq = bf16(scale dQ).  Under the causal mask query tile i
 // visits key tiles 0..i only (tiles wholly in the future are skipped).
 //
-// Warps: 0-3 one query row per thread, 4 TMA producer, 5 MMA issuer.
-// Tensor memory: S [0,128) (dS as bf16 over its first 64 columns),
-// dP [128,256), dQ [256, 256+DP).
+// Pipeline: S_j goes to one of two tensor-memory S buffers (j mod 2) and dP_j
+// to a single dP buffer.  The row warps load S_j and dP_j, release the dP
+// buffer at once (dP_{j+1} is computed while they work), turn the values into
+// dS_j and write it as bf16 over the S columns they have read; then dQ_j
+// reads it and S_{j+2} takes the buffer.  S_{j+1} was computed one tile
+// ahead, so the threads and the tensor core work at the same time.  No row
+// reduction is needed (P comes from the saved L), so each query row is split
+// between two warps, 64 key columns each.
+//
+// Warps: 0-7 query rows (warp w: rows 32 (w % 4).., key columns 64 (w / 4)..),
+// 8 TMA producer, 9 MMA issuer and tensor-memory owner.
+// Tensor memory: S buffers [0,128) and [128,256) (dS as bf16 pairs at columns
+// 64g.. over the S columns warp group g read), dP [256,384), dQ [384, 384+DP).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -42,27 +52,35 @@ struct DqCfg {
   static constexpr int SUB = DP / 64;
   static constexpr int SUB_BYTES = 128 * 128;
   static constexpr int TILE = SUB * SUB_BYTES;   // 128 x DP bf16
-  static constexpr int NS = (D == 64) ? 4 : 2;   // K/V ring stages
+  // K_j is read by S_j and dQ_j, and S_{j+2} is issued right after dQ_j:
+  // three K stages let K_{j+2} arrive while K_j and K_{j+1} are in use.
+  // V_j is read by dP_j only.
+  static constexpr int NSK = (D == 64) ? 4 : 3;
+  static constexpr int NSV = (D == 64) ? 4 : 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + TILE;
   static constexpr int OFF_K = OFF_DO + TILE;
-  static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  static constexpr int OFF_V = OFF_K + NSK * TILE;
+  static constexpr int OFF_BAR = OFF_V + NSV * TILE;
   static constexpr int B_QD = 0;
-  static constexpr int B_KFULL = 1;
-  static constexpr int B_KEMPTY = B_KFULL + NS;
-  static constexpr int B_VFULL = B_KEMPTY + NS;
-  static constexpr int B_VEMPTY = B_VFULL + NS;
-  static constexpr int B_SFULL = B_VEMPTY + NS;   // S and dP of a tile in TMEM
-  static constexpr int B_DSREADY = B_SFULL + 1;   // dS in TMEM (4 warp arrivals)
-  static constexpr int B_DQDONE = B_DSREADY + 1;  // every dQ MMA done (completes once)
+  static constexpr int B_KFULL = 1;                // [NSK]
+  static constexpr int B_KEMPTY = B_KFULL + NSK;   // [NSK]
+  static constexpr int B_VFULL = B_KEMPTY + NSK;   // [NSV]
+  static constexpr int B_VEMPTY = B_VFULL + NSV;   // [NSV]
+  static constexpr int B_SFULL = B_VEMPTY + NSV;   // [2] S_j in S buffer j % 2
+  static constexpr int B_DPFULL = B_SFULL + 2;     // dP_j in the dP buffer
+  static constexpr int B_DPFREE = B_DPFULL + 1;    // dP_j read by every row warp (8 arrivals)
+  static constexpr int B_DSREADY = B_DPFREE + 1;   // [2] dS_j in S buffer j % 2 (8 arrivals)
+  static constexpr int B_DQDONE = B_DSREADY + 2;   // every dQ MMA done (completes once)
   static constexpr int B_DRAIN = B_DQDONE + 1;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
+  static constexpr uint32_t COL_S = 0, COL_DP = 256, COL_DQ = 384;  // S buffer b at COL_S + 128 b
+  static_assert(COL_DQ + DP <= TMEM_COLS, "tensor memory");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 struct DqParams {
@@ -76,7 +94,7 @@ struct DqParams {
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV,
@@ -106,20 +124,26 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_QD), 1);
-    for (int s = 0; s < C::NS; ++s) {
+    for (int s = 0; s < C::NSK; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
       mbar_init(bar(C::B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::NSV; ++s) {
       mbar_init(bar(C::B_VFULL + s), 1);
       mbar_init(bar(C::B_VEMPTY + s), 1);
     }
-    mbar_init(bar(C::B_SFULL), 1);
-    mbar_init(bar(C::B_DSREADY), 4);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(bar(C::B_SFULL + b2), 1);
+      mbar_init(bar(C::B_DSREADY + b2), 8);
+    }
+    mbar_init(bar(C::B_DPFULL), 1);
+    mbar_init(bar(C::B_DPFREE), 8);
     mbar_init(bar(C::B_DQDONE), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -133,7 +157,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sK = sbase + C::OFF_K;
   const uint32_t sV = sbase + C::OFF_V;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
       tma_prefetch_desc(&tmQ);
@@ -146,37 +170,40 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_3d(sQ + s * C::SUB_BYTES, &tmQ, bar(C::B_QD), 64 * s, qt * C::BM, bh);
         tma_load_3d(sdO + s * C::SUB_BYTES, &tmdO, bar(C::B_QD), 64 * s, qt * C::BM, bh);
       }
-      int issued = 0;
+      // K_j then V_j, in the order the products need them (S_j comes before dP_j).
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j % C::NS;
-        const uint32_t ph = ((j / C::NS) - 1) & 1;
-        if (j >= C::NS &&
-            !mbar_wait(bar(C::B_KEMPTY + st), ph, abort_flag, p.err, kErrTimeoutLoad))
+        const int sk = j % C::NSK;
+        if (j >= C::NSK && !mbar_wait(bar(C::B_KEMPTY + sk), ((j / C::NSK) - 1) & 1, abort_flag,
+                                      p.err, kErrTimeoutLoad))
           break;
-        mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE);
+        mbar_arrive_expect_tx(bar(C::B_KFULL + sk), C::TILE);
 #pragma unroll
         for (int s = 0; s < C::SUB; ++s)
-          tma_load_3d(sK + st * C::TILE + s * C::SUB_BYTES, &tmK, bar(C::B_KFULL + st), 64 * s,
+          tma_load_3d(sK + sk * C::TILE + s * C::SUB_BYTES, &tmK, bar(C::B_KFULL + sk), 64 * s,
                       j * C::BN, kvz);
-        if (j >= C::NS &&
-            !mbar_wait(bar(C::B_VEMPTY + st), ph, abort_flag, p.err, kErrTimeoutLoad))
+        k_issued = j + 1;
+        const int sv = j % C::NSV;
+        if (j >= C::NSV && !mbar_wait(bar(C::B_VEMPTY + sv), ((j / C::NSV) - 1) & 1, abort_flag,
+                                      p.err, kErrTimeoutLoad))
           break;
-        mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE);
+        mbar_arrive_expect_tx(bar(C::B_VFULL + sv), C::TILE);
 #pragma unroll
         for (int s = 0; s < C::SUB; ++s)
-          tma_load_3d(sV + st * C::TILE + s * C::SUB_BYTES, &tmV, bar(C::B_VFULL + st), 64 * s,
+          tma_load_3d(sV + sv * C::TILE + s * C::SUB_BYTES, &tmV, bar(C::B_VFULL + sv), 64 * s,
                       j * C::BN, kvz);
-        issued = j + 1;
+        v_issued = j + 1;
       }
       if (*abort_flag) {
+        // Let the copies in flight land before the CTA exits.
         mbar_wait_timed(bar(C::B_QD), 0);
-        for (int j = max(0, issued - C::NS); j < issued; ++j) {
-          mbar_wait_timed(bar(C::B_KFULL + j % C::NS), (j / C::NS) & 1);
-          mbar_wait_timed(bar(C::B_VFULL + j % C::NS), (j / C::NS) & 1);
-        }
+        for (int j = max(0, k_issued - C::NSK); j < k_issued; ++j)
+          mbar_wait_timed(bar(C::B_KFULL + j % C::NSK), (j / C::NSK) & 1);
+        for (int j = max(0, v_issued - C::NSV); j < v_issued; ++j)
+          mbar_wait_timed(bar(C::B_VFULL + j % C::NSV), (j / C::NSV) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);  // S, dP
@@ -187,44 +214,72 @@ __global__ void __launch_bounds__(192, 1)
       const uint64_t v_kmaj = smem_desc_sw128(sV, 16, 1024);
       const uint64_t k_mn = smem_desc_sw128(sK, C::SUB_BYTES, 1024);
       bool ok = mbar_wait(bar(C::B_QD), 0, abort_flag, p.err, kErrTimeoutMma);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % C::NS;
-        if (!mbar_wait(bar(C::B_KFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
-          break;
+      // S_j = Q K_j^T into S buffer j % 2.
+      auto issue_s = [&](int j) -> bool {
+        const int sk = j % C::NSK;
+        if (!mbar_wait(bar(C::B_KFULL + sk), (j / C::NSK) & 1, abort_flag, p.err, kErrTimeoutMma))
+          return false;
         tc_fence_after();
-        const uint64_t kd = desc_add(k_kmaj, st * C::TILE);
-        mma_ss_k<ID_S, 0>(tmem + C::COL_S, q_desc, kd);
+        const uint32_t dst = tmem + C::COL_S + 128 * (j & 1);
+        const uint64_t kd = desc_add(k_kmaj, sk * C::TILE);
+        mma_ss_k<ID_S, 0>(dst, q_desc, kd);
 #pragma unroll
         for (int kk = 1; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          mma_ss_k<ID_S, 1>(tmem + C::COL_S, desc_add(q_desc, off), desc_add(kd, off));
+          mma_ss_k<ID_S, 1>(dst, desc_add(q_desc, off), desc_add(kd, off));
         }
-        if (!mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
-          break;
+        mma_commit(bar(C::B_SFULL + (j & 1)));
+        return true;
+      };
+      // dP_j = dO V_j^T into the dP buffer.
+      auto issue_dp = [&](int j) -> bool {
+        const int sv = j % C::NSV;
+        if (!mbar_wait(bar(C::B_VFULL + sv), (j / C::NSV) & 1, abort_flag, p.err, kErrTimeoutMma))
+          return false;
         tc_fence_after();
-        const uint64_t vd = desc_add(v_kmaj, st * C::TILE);
+        const uint64_t vd = desc_add(v_kmaj, sv * C::TILE);
         mma_ss_k<ID_S, 0>(tmem + C::COL_DP, do_desc, vd);
 #pragma unroll
         for (int kk = 1; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
           mma_ss_k<ID_S, 1>(tmem + C::COL_DP, desc_add(do_desc, off), desc_add(vd, off));
         }
-        mma_commit(bar(C::B_SFULL));
-        mma_commit(bar(C::B_VEMPTY + st));
-        if (!mbar_wait(bar(C::B_DSREADY), j & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+        mma_commit(bar(C::B_DPFULL));
+        mma_commit(bar(C::B_VEMPTY + sv));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok) ok = issue_dp(0);
+      if (ok && n_kv > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        // dP_{j+1} as soon as the row warps hold dP_j in registers.
+        if (j + 1 < n_kv) {
+          if (!mbar_wait(bar(C::B_DPFREE), j & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+          tc_fence_after();
+          if (!issue_dp(j + 1)) break;
+        }
+        if (!mbar_wait(bar(C::B_DSREADY + (j & 1)), (j >> 1) & 1, abort_flag, p.err,
+                       kErrTimeoutMma))
+          break;
         tc_fence_after();
-        // dQ += dS K_j: dS packed in S's first 64 columns, 16 keys = 8 columns per step;
-        // K_j read MN-major, 16 key rows (2 KB) per step.
-        const uint64_t kmn = desc_add(k_mn, st * C::TILE);
+        // dQ += dS_j K_j.  dS of keys 64g.. sits packed (bf16 pairs) at
+        // columns 64g.. of the S buffer, 16 keys = 8 columns per step; K_j is
+        // read MN-major, 16 key rows (2 KB) per step.
+        const int sk = j % C::NSK;
+        const uint32_t sb = tmem + C::COL_S + 128 * (j & 1);
+        const uint64_t kmn = desc_add(k_mn, sk * C::TILE);
         if (j == 0)
-          mma_ts_k<ID_Q, 0>(tmem + C::COL_DQ, tmem + C::COL_S, kmn);
+          mma_ts_k<ID_Q, 0>(tmem + C::COL_DQ, sb, kmn);
         else
-          mma_ts_k<ID_Q, 1>(tmem + C::COL_DQ, tmem + C::COL_S, kmn);
+          mma_ts_k<ID_Q, 1>(tmem + C::COL_DQ, sb, kmn);
 #pragma unroll
         for (int kk = 1; kk < 8; ++kk)
-          mma_ts_k<ID_Q, 1>(tmem + C::COL_DQ, tmem + C::COL_S + kk * 8,
+          mma_ts_k<ID_Q, 1>(tmem + C::COL_DQ, sb + (kk >> 2) * 64 + (kk & 3) * 8,
                             desc_add(kmn, kk * 2048));
-        mma_commit(bar(C::B_KEMPTY + st));
+        mma_commit(bar(C::B_KEMPTY + sk));
+        // S_{j+2} reuses this S buffer; the products run in issue order, so it
+        // overwrites dS_j only after dQ_j has read it.
+        if (j + 2 < n_kv && !issue_s(j + 2)) break;
         // Once, after the last tile: a barrier that completed once per tile
         // could not tell its last phase from an earlier one by parity alone.
         if (j == n_kv - 1) mma_commit(bar(C::B_DQDONE));
@@ -236,60 +291,76 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ query rows
+    // Warp w reads tensor-memory lanes 32 (w % 4) .. +31 (its query rows)
+    // and key columns 64 (w / 4) .. +63 of each tile.
     grid_dependency_wait();  // D comes from the row-dot pass, before the dK/dV grid
-    const int row = threadIdx.x;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int wq = warp & 3, g = warp >> 2;
+    const int row = wq * 32 + static_cast<int>(threadIdx.x & 31);
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const int qi = qt * C::BM + row;
     const bool live = qi < p.N;
     const size_t ridx = static_cast<size_t>(bh) * p.N + (live ? qi : 0);
     const float L2 = live ? p.lse[ridx] * kLog2e : INFINITY;  // dead rows: P = 0
     const float Drow = live ? p.Dvec[ridx] : 0.0f;
-    const float c = p.scale_log2;
+    const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t nl2 = f2_pack(-L2, -L2);
+    const uint64_t nd2 = f2_pack(-Drow, -Drow);
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL), j & 1, abort_flag, p.err,
-                                             kErrTimeoutSoftmax));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + (j & 1)), (j >> 1) & 1, abort_flag,
+                                             p.err, kErrTimeoutSoftmax));
+      if (ok)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DPFULL), j & 1, abort_flag, p.err,
+                                               kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
-      const int kbase = j * C::BN;
-      const bool need_mask = __any_sync(
-          0xffffffffu, (kbase + C::BN > p.N) || (CAUSAL && kbase + C::BN - 1 > qt * C::BM));
+      const uint32_t scol = C::COL_S + 128 * (j & 1) + 64 * g;
+      uint32_t sv[64], dpv[64];
+      tmem_ld32(tmem + lane_off + scol, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(tmem + lane_off + scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld32(tmem + lane_off + C::COL_DP + 64 * g, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
+      tmem_ld32(tmem + lane_off + C::COL_DP + 64 * g + 32,
+                *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive_warp(bar(C::B_DPFREE));
+      const int kbase = j * C::BN + 64 * g;
+      const bool need_mask = (kbase + 64 > p.N) || (CAUSAL && kbase + 63 > qt * C::BM);
+      uint32_t pk[32];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(tmem + lane_off + C::COL_S + cc * 32, sv);
-        tmem_ld32(tmem + lane_off + C::COL_DP + cc * 32, dpv);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float pr = ex2_approx(fmaf(__uint_as_float(sv[2 * u + e]), c, -L2));
-            if (need_mask) {
-              const int key = kbase + cc * 32 + 2 * u + e;
-              if (key >= p.N || (CAUSAL && key > qi)) pr = 0.0f;
-            }
-            ds[e] = pr * (__uint_as_float(dpv[2 * u + e]) - Drow);
-          }
-          pk[u] = pack_bf16x2(ds[0], ds[1]);
+      for (int u = 0; u < 32; ++u) {
+        float p0, p1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * u]), __uint_as_float(sv[2 * u + 1])),
+                         c2, nl2),
+                  p0, p1);
+        p0 = ex2_approx(p0);
+        p1 = ex2_approx(p1);
+        if (need_mask) {
+          const int key = kbase + 2 * u;
+          if (key >= p.N || (CAUSAL && key > qi)) p0 = 0.0f;
+          if (key + 1 >= p.N || (CAUSAL && key + 1 > qi)) p1 = 0.0f;
         }
-        // dS (bf16) over S columns already read: keys cc*32.. -> columns cc*16..
-        tmem_st16(tmem + lane_off + C::COL_S + cc * 16, pk);
+        const uint64_t dd =
+            f2_add(f2_pack(__uint_as_float(dpv[2 * u]), __uint_as_float(dpv[2 * u + 1])), nd2);
+        float d0, d1;
+        f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
+        pk[u] = pack_bf16x2(d0, d1);
       }
+      // dS (bf16 pairs) over S columns this warp has already read.
+      tmem_st32(tmem + lane_off + scol, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(bar(C::B_DSREADY));
+      mbar_arrive_warp(bar(C::B_DSREADY + (j & 1)));
     }
-    // ---- epilogue: dq = bf16(scale dQ), one row per thread
+    // ---- epilogue: dq = bf16(scale dQ), one row per thread, 32-column
+    // chunks split between the two warps of a row
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQDONE), 0, abort_flag, p.err,
                                                    kErrTimeoutEpilogue));
     if (ok) {
       tc_fence_after();
       __nv_bfloat16* qrow = p.dq + ridx * D;
-#pragma unroll
-      for (int q4 = 0; q4 < D / 32; ++q4) {
+#pragma unroll 1
+      for (int q4 = g; q4 < D / 32; q4 += 2) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + C::COL_DQ + q4 * 32, r);
         tmem_wait_ld();
@@ -313,7 +384,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
