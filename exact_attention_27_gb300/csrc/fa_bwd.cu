@@ -454,12 +454,23 @@ __global__ void __launch_bounds__(384, 1)
       // Masking is needed only on the diagonal tile and for keys past N.
       const bool masked = __any_sync(0xffffffffu, (CAUSAL && it == jt) || !key_live);
       const uint64_t c2 = f2_pack(c, c);
+      // Chunk cc + 1 (32 query columns of S^T and dP^T) is loaded while
+      // chunk cc is computed: tcgen05.wait::ld waits for every load issued,
+      // so each wait covers only loads that had a chunk's arithmetic to land.
+      // The P^T of chunk cc goes to columns 16cc.., below the S^T columns
+      // 32(cc + 1).. being loaded.
+      uint32_t sv2[2][32], dpv2[2][32];
+      tmem_ld32(tmem + lane_off + C::COL_S, sv2[0]);
+      tmem_ld32(tmem + lane_off + C::COL_DP, dpv2[0]);
+      tmem_wait_ld();
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(tmem + lane_off + C::COL_S + cc * 32, sv);
-        tmem_ld32(tmem + lane_off + C::COL_DP + cc * 32, dpv);
-        tmem_wait_ld();
+        if (cc + 1 < 4) {
+          tmem_ld32(tmem + lane_off + C::COL_S + (cc + 1) * 32, sv2[(cc + 1) & 1]);
+          tmem_ld32(tmem + lane_off + C::COL_DP + (cc + 1) * 32, dpv2[(cc + 1) & 1]);
+        }
+        const uint32_t(&sv)[32] = sv2[cc & 1];
+        const uint32_t(&dpv)[32] = dpv2[cc & 1];
         uint32_t pk[16], dk16[16];
 #pragma unroll
         for (int u4 = 0; u4 < 8; ++u4) {
@@ -506,6 +517,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int q4 = 0; q4 < 4; ++q4)
           st_shared_v4(blk + sw128(t, (cc & 1) * 4 + q4), dk16[4 * q4], dk16[4 * q4 + 1],
                        dk16[4 * q4 + 2], dk16[4 * q4 + 3]);
+        if (cc + 1 < 4) tmem_wait_ld();
       }
       tmem_wait_st();
       fence_proxy_async_smem();
