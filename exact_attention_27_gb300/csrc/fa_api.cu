@@ -128,6 +128,11 @@ bool encode_map_f32_acc(CUtensorMap* m, const void* ptr, int d, int N, long long
                   CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+bool encode_map_f32_acc32(CUtensorMap* m, const void* ptr, int d, int N, long long planes) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, d, N, planes, 32, 32,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 }  // namespace fa
 
 extern "C" {
@@ -250,7 +255,9 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
             make_map_bf16(&m.v, v, d, N, static_cast<long long>(B) * H_kv) &&
             make_map_bf16(&m.dO, dO, d, N, static_cast<long long>(B) * H_q) &&
             make_map(&m.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, d, N,
-                     static_cast<long long>(B) * H_q, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+                     static_cast<long long>(B) * H_q, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&m.dq_acc32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, d, N,
+                     static_cast<long long>(B) * H_q, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
   cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
   if (e == cudaSuccess) e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream, acc);

@@ -128,15 +128,16 @@ struct BwdCfg {
   static constexpr int SUB_BYTES = 128 * 128;
   static constexpr int TILE = SUB * SUB_BYTES;  // 128 x DP bf16
   // Q has two stages, so that S^T of the next step needs no load; dO has one,
-  // released as soon as dV has read it.  dQ leaves through one staging box of
-  // 128 rows x 32 fp32, refilled once the previous reduce has read it.
+  // released as soon as dV has read it.  dQ leaves through a 16 KB staging
+  // tile, one 32 x 32 fp32 box per drain warp, each refilled once that warp's
+  // previous reduce has read it.
   static constexpr int NQ = 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
   static constexpr int OFF_Q = OFF_V + TILE;
   static constexpr int OFF_DO = OFF_Q + NQ * TILE;
   static constexpr int OFF_DS = OFF_DO + TILE;    // dS^T: 128 keys x 128 queries bf16
-  static constexpr int OFF_STG = OFF_DS + 2 * SUB_BYTES;  // dQ staging: one box 128 x 32 fp32
+  static constexpr int OFF_STG = OFF_DS + 2 * SUB_BYTES;  // dQ staging: 4 x (32 rows x 32 fp32)
   static constexpr int OFF_LD = OFF_STG + SUB_BYTES;     // -L log2e [2][128], -D [2][128]
   static constexpr int OFF_BAR = OFF_LD + 4 * 128 * 4;
   static constexpr int B_KV = 0;
@@ -149,8 +150,7 @@ struct BwdCfg {
   static constexpr int B_DQFULL = B_PDS + 1;      // dQ in TMEM, all MMAs of the step done
   static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ columns drained (128 arrivals)
   static constexpr int B_WG = B_DQFREE + 1;      // key-row warpgroup sync (128 arrivals)
-  static constexpr int B_WG2 = B_WG + 1;         // drain warpgroup sync (128 arrivals)
-  static constexpr int B_DRAIN = B_WG2 + 1;
+  static constexpr int B_DRAIN = B_WG + 1;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -265,7 +265,6 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQFREE), 128);
     mbar_init(bar(C::B_WG), 128);
-    mbar_init(bar(C::B_WG2), 128);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -542,26 +541,24 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ dQ drain
     // dQ of step s sits in dP^T's columns: take all of it into registers,
     // hand the columns back (the next dP^T may be computed), then reduce it
-    // into the fp32 accumulator through the staging tile, D / 32 boxes of
-    // 128 rows x 32 fp32, one at a time.  The accumulator was zeroed by the
-    // row-dot pass (the grid before this one).
+    // into the fp32 accumulator, D / 32 boxes of 32 columns.  Each warp
+    // stages its own 32 rows (4 KB of the staging tile) and its lane 0
+    // issues the reduce of that 32 x 32 box, so no warp waits for another;
+    // a warp refills its slice once its own previous reduce has read it.
+    // The accumulator was zeroed by the row-dot pass (the grid before).
     grid_dependency_wait();
     const int t = threadIdx.x & 127;  // query row of the step's tile
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t wg_phase = 0;
+    const int wq = warp & 3;
+    const int r = t & 31;             // row within this warp's box
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t sW = sSTG + wq * 4096;
     bool ok = true;
-    auto wg_sync = [&]() -> bool {
-      mbar_arrive(bar(C::B_WG2));
-      const bool r = mbar_wait(bar(C::B_WG2), wg_phase & 1, abort_flag, p.err, kErrTimeoutOther);
-      ++wg_phase;
-      return __all_sync(0xffffffffu, r);
-    };
     constexpr int kBoxes = D / 32;
     for (int s = 0; s < n_steps; ++s) {
       const int g = s / per_head;
       const int it = i0 + (s - g * per_head);
       const int bhq = b * p.Hq + hkv * p.G + g;
-      const int q0 = it * C::BQ;
+      const int y0 = it * C::BQ + 32 * wq;  // first query row of this warp's box
       ok = __all_sync(0xffffffffu,
                       mbar_wait(bar(C::B_DQFULL), s & 1, abort_flag, p.err, kErrTimeoutOther));
       if (!ok) break;
@@ -574,22 +571,23 @@ __global__ void __launch_bounds__(384, 1)
       }
       tc_fence_before();
       mbar_arrive(bar(C::B_DQFREE));  // dP^T's columns may be overwritten now
+      // Rows at or past N are not reduced (a box starting there is skipped).
+      const bool box_live = y0 < p.N;
 #pragma unroll
       for (int x = 0; x < (DQ ? kBoxes : 0); ++x) {
-        if (t == 0) bulk_wait_group_read0();  // staging free again
-        if (!(ok = wg_sync())) break;
+        if (r == 0) bulk_wait_group_read0();  // this warp's slice is free again
+        __syncwarp();
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
-          st_shared_v4(sSTG + sw128(t, ch), dqv[x][4 * ch], dqv[x][4 * ch + 1], dqv[x][4 * ch + 2],
+          st_shared_v4(sW + sw128(r, ch), dqv[x][4 * ch], dqv[x][4 * ch + 1], dqv[x][4 * ch + 2],
                        dqv[x][4 * ch + 3]);
         fence_proxy_async_smem();
-        if (!(ok = wg_sync())) break;
-        if (t == 0) {
-          tma_reduce_add_3d(&tmdQ, sSTG, x * 32, q0, bhq);
+        __syncwarp();
+        if (r == 0 && box_live) {
+          tma_reduce_add_3d(&tmdQ, sW, x * 32, y0, bhq);
           bulk_commit_group();
         }
       }
-      if (!ok) break;
     }
     // dV, once the last step's products have completed (its dQ commit, which
     // the loop waited for, covers them); the key-row warpgroup writes dK.
@@ -604,7 +602,7 @@ __global__ void __launch_bounds__(384, 1)
     // Only the staging tile's reads must be over before the CTA's shared
     // memory is released; the reduces' writes complete on their own, and the
     // dQ finalisation reads the accumulator only after this grid has completed.
-    if (t == 0) bulk_wait_group_read0();
+    if (r == 0) bulk_wait_group_read0();
     __syncwarp();
     grid_launch_dependents();  // the dQ finalisation may be scheduled
   }
@@ -674,7 +672,7 @@ cudaError_t launch_bwd_t(const BwdMaps& m, const float* lse, const float* Dv, vo
   const int n_ktiles = (s.N + C::BK - 1) / C::BK;
   dim3 grid(static_cast<unsigned>(s.B * s.Hkv), static_cast<unsigned>(n_ktiles));
   return launch_dependent(kern, grid, dim3(C::THREADS), C::SMEM_BYTES, stream, m.q, m.k, m.v,
-                          m.dO, m.dq_acc, p);
+                          m.dO, m.dq_acc32, p);
 }
 
 cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* Dv, float*, void* dk,

@@ -91,6 +91,7 @@ cudaError_t launch_preprocess(const void* o, const void* dO, float* D, long long
 struct BwdMaps {
   CUtensorMap q, k, v, dO;  // bf16, box 64 x 128 x 1, 128-byte swizzle
   CUtensorMap dq_acc;       // fp32 accumulator, box 32 x 128 x 1, 128-byte swizzle
+  CUtensorMap dq_acc32;     // the same accumulator, box 32 x 32 x 1 (one warp's rows)
 };
 
 // Head dimension 64 (fa_bwd_d64.cu); launch_backward dispatches to it.
@@ -115,6 +116,7 @@ cudaError_t launch_backward_dq(const BwdMaps& m, const float* lse, const float* 
 uint32_t* device_error_word();
 bool encode_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long planes);
 bool encode_map_f32_acc(CUtensorMap* m, const void* ptr, int d, int N, long long planes);
+bool encode_map_f32_acc32(CUtensorMap* m, const void* ptr, int d, int N, long long planes);
 
 cudaError_t launch_dq_finalize(const float* dq_acc, void* dq, long long n, float scale,
                                cudaStream_t stream);

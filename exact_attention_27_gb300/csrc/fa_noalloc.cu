@@ -84,7 +84,8 @@ extern "C" fa_status fa_backward_noalloc(const void* q, const void* k, const voi
                   fa::encode_map_bf16(&m.k, k, d, N, static_cast<long long>(B) * H_kv) &&
                   fa::encode_map_bf16(&m.v, v, d, N, static_cast<long long>(B) * H_kv) &&
                   fa::encode_map_bf16(&m.dO, dO, d, N, static_cast<long long>(B) * H_q) &&
-                  fa::encode_map_f32_acc(&m.dq_acc, acc, d, N, static_cast<long long>(B) * H_q);
+                  fa::encode_map_f32_acc(&m.dq_acc, acc, d, N, static_cast<long long>(B) * H_q) &&
+                  fa::encode_map_f32_acc32(&m.dq_acc32, acc, d, N, static_cast<long long>(B) * H_q);
   if (!ok) return FA_ERR_CUDA;
   fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
   // The accumulator keeps the previous call's sums: the preprocess clears it.
