@@ -198,7 +198,8 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
 #define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 /*
- * fa_backward without any device allocation (the paper has no counterpart).
+ * fa_backward without any device allocation (an addition of this library;
+ * the source pages describe no such entry point).
  *
  * For callers that cannot allocate device memory at the point where they
  * run the backward pass: for example an application whose device memory is
