@@ -173,6 +173,8 @@ def test_deterministic_backward_is_bitwise_reproducible(d, G):
     (2, 16, 16, 4096, 96, False),    # the d = 96 one
     (1, 8, 2, 4096, 128, False),     # grouped-query heads at full length
     (2, 16, 16, 4096, 128, True),    # the deterministic path at the same size
+    (1, 2, 2, 32768, 64, False),     # long sequence: 256 query tiles for the first key tile
+    (1, 2, 2, 32768, 64, True),      # and the deterministic path there
 ])
 def test_full_size_backward_sampled(B, Hq, Hkv, N, d, det):
     """Full-size causal backward against the oracle on two 256-row query
