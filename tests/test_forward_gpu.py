@@ -258,3 +258,18 @@ def test_tile_rows_rejects_other_values():
     with pytest.raises(fa.FaError):
         fa.fa_set_forward_tile_rows(64)
     fa.fa_set_forward_tile_rows(0)
+
+
+@pytest.mark.parametrize("rows_per_cta", [128, 256])
+@pytest.mark.parametrize("d", [64, 96, 128, 256])
+def test_long_sequence_one_head(tile_rows, rows_per_cta, d):
+    """N = 32768, one head: the last query tile visits 256 key tiles (512 at
+    d = 256, whose key tiles have 64 rows).  Both tile sizes (d = 256 always
+    runs one tile per CTA); tile edges plus seeded rows against the oracle."""
+    tile_rows(rows_per_cta)
+    N = 32768
+    inp = make_inputs(1, 1, 1, N, d, seed=d + rows_per_cta)
+    rng = np.random.default_rng(d)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, N - 129, N - 128, N - 1],
+                                     rng.integers(0, N, 16)]))
+    forward_vs_oracle(inp, True, 1.0 / math.sqrt(d), rows=rows)
