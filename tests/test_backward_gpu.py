@@ -211,3 +211,26 @@ def test_full_size_backward_sampled(B, Hq, Hkv, N, d, det):
             assert np.isfinite(g).all()
             err = np.abs(g - r).max()
             assert err <= GRAD_REL * np.abs(r).max(), f"rows {r0}..: err {err:.3e}"
+
+
+@pytest.mark.parametrize("d", [64, 96, 128])
+@pytest.mark.parametrize("det", [False, True])
+def test_many_heads_tiny_sequence(d, det):
+    """B x H_q = 4096 heads of 17 positions, GQA 2: every CTA holds one
+    partial tile (and the forward's second tile of a pair lies wholly past
+    N).  Forward and gradients, every row, against the oracle."""
+    import exact_attention_27_gb300 as fa
+    B, Hq, Hkv, N = 64, 64, 32, 17
+    inp = make_inputs(B, Hq, Hkv, N, d, seed=d + det, with_grad=True)
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=scale)
+    grads = fa.attention_backward(q, k, v, o, lse, do, causal=True, scale=scale,
+                                  deterministic=det)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == 0
+    f = {n: as_f64(inp[n]) for n in ("q", "k", "v", "do")}
+    o_ref, l_ref = oracle.attention_forward(f["q"], f["k"], f["v"], scale, True)
+    check_forward(o, lse, o_ref, l_ref, "many heads")
+    ref = oracle.attention_backward(f["q"], f["k"], f["v"], f["do"], scale, True)
+    check_grads(grads, ref, "many heads")
