@@ -281,6 +281,9 @@ def run_ours(args, rank, world):
             result["fwd_workloads"] = forward_workloads(fa, torch, tflops_peak, peak_src)
             result["fwd_workloads"].append(forward_fp8_workload(fa, torch, tflops_peak, peak_src))
             result["bwd_workloads"] = backward_workloads(fa, torch, tflops_peak, peak_src)
+            result["preprocess"] = [preprocess_workload(fa, torch, w, hbm_peak, peak_src),
+                                    preprocess_workload(fa, torch, WORKLOADS["causal_n8192_d128"],
+                                                        hbm_peak, peak_src)]
             result["e2e"] = end_to_end(fa, torch, w, min(K, 50))
             if world == 1:
                 result["cpu_baseline"] = cpu_baseline(w, gpu_out)
@@ -478,6 +481,34 @@ def run_tile_rows_sweep(args):
         fa.fa_set_forward_tile_rows(0)
     return {"sweep": "forward tile rows", "shapes": n_shapes, "sms": sms,
             "summed_loss_vs_faster": round(lost, 3)}
+
+
+def preprocess_workload(fa, torch, w, hbm_peak, peak_src):
+    """The row-dot pass D = rowsum(dO o O) (fa_backward_preprocess) alone on
+    the step's shapes: memory-bound, reported in GB/s against the copy
+    bandwidth.  Algorithmic bytes: O and dO read once, D written.  Each launch
+    reads a different input set, enough sets that together they exceed L2 by
+    3x, so every launch reads from HBM; per-launch CUDA events."""
+    rows = w.B * w.Hq * w.N
+    nbytes = 2 * rows * w.d * 2 + rows * 4
+    nset = _rotation(2 * rows * w.d * 2)
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    sets = []
+    for _ in range(nset):
+        o = torch.randn(w.B, w.Hq, w.N, w.d, device="cuda", generator=gen).to(torch.bfloat16)
+        do = torch.randn(w.B, w.Hq, w.N, w.d, device="cuda", generator=gen).to(torch.bfloat16)
+        D = torch.empty(w.B, w.Hq, w.N, device="cuda", dtype=torch.float32)
+        sets.append((o, do, D))
+    for i in range(3):
+        fa.fa_backward_preprocess(*sets[i % nset])
+    t = per_launch_ms(torch, lambda i: fa.fa_backward_preprocess(*sets[i % nset]),
+                      reps=max(20, nset))
+    gbs = nbytes / (t["median"] * 1e-3) / 1e9
+    del sets
+    return {"kernel": "preprocess_kernel<%d>" % w.d, "workload": w.describe(),
+            "bytes_per_launch": nbytes, "input_sets": nset, "per_launch_ms": t,
+            "achieved_gbs": round(gbs, 1), "peak_gbs": hbm_peak, "frac": round(gbs / hbm_peak, 4),
+            "peak_source": f"{peak_src} copy"}
 
 
 def forward_workloads(fa, torch, tflops_peak, peak_src):
