@@ -408,14 +408,7 @@ cudaError_t launch_dq_t(const BwdMaps& m, const float* lse, const float* Dv, voi
   p.n_qtiles = (s.N + C::BM - 1) / C::BM;
   p.n_ktiles = (s.N + C::BN - 1) / C::BN;
   p.n_heads = s.B * s.Hq;
-  {
-    const double kv_bytes = 2.0 * s.N * D * 2.0;
-    long long kv_heads = static_cast<long long>(48.0 * 1024 * 1024 / kv_bytes);
-    if (kv_heads < 1) kv_heads = 1;
-    long long hpg = kv_heads * p.G;
-    if (hpg > p.n_heads) hpg = p.n_heads;
-    p.heads_per_group = static_cast<int>(hpg);
-  }
+  p.heads_per_group = static_cast<int>(heads_per_group(s.N, D, 2.0, p.G, p.n_heads));
   p.scale = s.scale;
   p.scale_log2 = s.scale * kLog2e;
   p.err = err;

@@ -636,17 +636,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   p.o_scale = o_scale;
   p.err = err;
   p.n_heads = s.B * s.Hq;
-  {
-    // Group query heads so that the K/V they read (shared within a GQA
-    // group) stays within about 48 MiB of the 129 MB L2.
-    const double kv_bytes = 2.0 * p.Nk * D * (FP8 ? 1.0 : 2.0);  // one K/V head
-    const double budget = 48.0 * 1024 * 1024;
-    long long kv_heads = static_cast<long long>(budget / kv_bytes);
-    if (kv_heads < 1) kv_heads = 1;
-    long long hpg = kv_heads * p.G;
-    if (hpg > p.n_heads) hpg = p.n_heads;
-    p.heads_per_group = static_cast<int>(hpg);
-  }
+  p.heads_per_group =
+      static_cast<int>(heads_per_group(p.Nk, D, FP8 ? 1.0 : 2.0, p.G, p.n_heads));
   const long long grid = static_cast<long long>(s.B) * s.Hq * p.n_qpairs;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   return launch_dependent(kern, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS), C::SMEM_BYTES,
@@ -713,12 +704,8 @@ int forward_rows_for(const AttnShape& s, int sms) {
     const auto it = g_rows_cache.find(key);
     if (it != g_rows_cache.end()) return it->second;
   }
-  // Launch-order grouping of heads, as both kernels' hosts size it: K/V of
-  // a group within about 48 MiB of L2, whole GQA groups.
-  const double kv_bytes = 2.0 * s.keys() * s.d * 2.0;
-  long long hpg = std::max(1LL, static_cast<long long>(48.0 * 1024 * 1024 / kv_bytes)) *
-                  (s.Hq / s.Hkv);
-  hpg = std::min(hpg, n_heads);
+  // Launch-order grouping of heads, as both kernels' launches size it.
+  const long long hpg = heads_per_group(s.keys(), s.d, 2.0, s.Hq / s.Hkv, n_heads);
   // Key tiles visited by query tile qt (the kernels' causal bound).
   auto tiles = [&](long long qt) -> double {
     if (qt >= n_qtiles) return 0.0;

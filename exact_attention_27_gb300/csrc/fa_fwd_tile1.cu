@@ -450,16 +450,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   p.n_heads = s.B * s.Hq;
   p.scale_log2 = s.scale * kLog2e;
   p.err = err;
-  {
-    // Group query heads so that the K/V they read stays within about 48 MiB
-    // of the 129 MB L2.
-    const double kv_bytes = 2.0 * p.Nk * C::D * 2.0;  // one K/V head
-    long long kv_heads = static_cast<long long>(48.0 * 1024 * 1024 / kv_bytes);
-    if (kv_heads < 1) kv_heads = 1;
-    long long hpg = kv_heads * p.G;
-    if (hpg > p.n_heads) hpg = p.n_heads;
-    p.heads_per_group = static_cast<int>(hpg);
-  }
+  p.heads_per_group = static_cast<int>(heads_per_group(p.Nk, C::D, 2.0, p.G, p.n_heads));
   const long long grid = static_cast<long long>(p.n_heads) * p.n_qtiles;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   return launch_dependent(kern, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS), C::SMEM_BYTES,

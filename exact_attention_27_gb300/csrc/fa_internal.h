@@ -75,6 +75,19 @@ cudaError_t set_smem_limit_once(int bytes) {
   return e;
 }
 
+// Launch-order grouping of query heads, shared by the forward kernels, the
+// dQ kernel and the forward's tile-size estimate: whole GQA groups whose K/V
+// (2 x keys x d elements of elem_bytes per K/V head) stay within about
+// 48 MiB of the 129 MB L2; at least one group of G heads, at most n_heads.
+inline long long heads_per_group(long long keys, int d, double elem_bytes, int G,
+                                 long long n_heads) {
+  const double kv_bytes = 2.0 * static_cast<double>(keys) * d * elem_bytes;
+  long long kv_heads = static_cast<long long>(48.0 * 1024 * 1024 / kv_bytes);
+  if (kv_heads < 1) kv_heads = 1;
+  const long long hpg = kv_heads * G;
+  return hpg < n_heads ? hpg : n_heads;
+}
+
 // Query rows per CTA for the forward: 0 = chosen per shape, 128 or 256.
 void set_forward_rows_per_cta(int rows);
 // Query rows per CTA (128 or 256) that the bf16 forward chooses for shape s
