@@ -287,7 +287,23 @@ def run_ours(args, rank, world):
             result["e2e"] = end_to_end(fa, torch, w, min(K, 50))
             if world == 1:
                 result["cpu_baseline"] = cpu_baseline(w, gpu_out)
+            result["summary"] = summary(result)
     return result
+
+
+def summary(result):
+    """The per-workload results in a few hundred characters, printed as the
+    last key of the line so that a reader that keeps only the end of the
+    output still sees them: [workload, ms, TFLOP/s, fraction of peak]."""
+    rows = [["step: " + result["config"]["workload"], result["ms_per_step"], result["value"],
+             result["config"]["frac_of_peak"]],
+            ["bwd main kernel (roofline)", result["bwd_main_kernel_ms"],
+             result["roofline"]["achieved"], result["roofline"]["frac"]]]
+    for key in ("fwd_workloads", "bwd_workloads"):
+        for x in result.get(key, []):
+            name = x["workload"].replace(" bf16", "").replace("e4m3 (O bf16)", "fp8")
+            rows.append([name, x["ms"], x["tflops"], x["frac"]])
+    return {"columns": ["workload", "ms", "TFLOP/s", "frac of measured peak"], "rows": rows}
 
 
 def _med_min(xs):

@@ -40,20 +40,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Device address of g_fa_error_word on the current device, cached per device.
-uint32_t* error_word() {
-  static uint32_t* cache[64] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<uint32_t*>(p);
-  }
-  return cache[dev];
-}
+// Device address of g_fa_error_word on the current device.
+uint32_t* error_word() { return static_cast<uint32_t*>(fa::symbol_address_cached(g_fa_error_word)); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -85,18 +73,6 @@ bool make_kv_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long p
                   d == 256 ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-fa_status validate(int B, int H_q, int H_kv, int N, int d, float scale, int causal) {
-  if (B < 1 || H_q < 1 || H_kv < 1 || N < 1) return FA_ERR_INVALID_ARGUMENT;
-  if (H_q % H_kv != 0) return FA_ERR_INVALID_ARGUMENT;
-  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARGUMENT;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARGUMENT;
-  if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
-  const double elems = static_cast<double>(B) * H_q * N * d;
-  if (elems >= 1099511627776.0) return FA_ERR_INVALID_ARGUMENT;  // 2^40
-  if ((N + 127) / 128 > 65535) return FA_ERR_INVALID_ARGUMENT;   // grid.y limit
-  return FA_OK;
-}
-
 // A single thread waits on an mbarrier that nothing will ever complete, with
 // the caller's time limit, then records the timeout like the real kernels do.
 __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, uint32_t* err) {
@@ -118,6 +94,18 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, uint32_t* err) {
 namespace fa {
 
 uint32_t* device_error_word() { return error_word(); }
+
+fa_status validate(int B, int H_q, int H_kv, int N, int d, float scale, int causal) {
+  if (B < 1 || H_q < 1 || H_kv < 1 || N < 1) return FA_ERR_INVALID_ARGUMENT;
+  if (H_q % H_kv != 0) return FA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARGUMENT;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARGUMENT;
+  if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  const double elems = static_cast<double>(B) * H_q * N * d;
+  if (elems >= 1099511627776.0) return FA_ERR_INVALID_ARGUMENT;  // 2^40
+  if ((N + 127) / 128 > 65535) return FA_ERR_INVALID_ARGUMENT;   // grid.y limit
+  return FA_OK;
+}
 
 bool encode_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long planes) {
   return make_map_bf16(m, ptr, d, N, planes);
@@ -141,7 +129,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
                      int H_q, int H_kv, int N, int d, float scale, int causal,
                      cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARGUMENT;
-  const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
+  const fa_status st = fa::validate(B, H_q, H_kv, N, d, scale, causal);
   if (st != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
@@ -162,7 +150,7 @@ fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, fl
                         int H_q, int H_kv, int N_q, int N_kv, int d, float scale, int causal,
                         int q_offset, cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARGUMENT;
-  fa_status st = validate(B, H_q, H_kv, N_q, d, scale, causal);
+  fa_status st = fa::validate(B, H_q, H_kv, N_q, d, scale, causal);
   if (st != FA_OK) return st;
   if (N_kv < 1 || q_offset < 0) return FA_ERR_INVALID_ARGUMENT;
   if (static_cast<double>(q_offset) + N_q + 128 >= 2147483647.0) return FA_ERR_INVALID_ARGUMENT;
@@ -188,7 +176,7 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o,
                          int B, int H_q, int H_kv, int N, int d, float scale, float q_descale,
                          float k_descale, float v_descale, int causal, cudaStream_t stream) {
   if (!q || !k || !v_t || !o || !lse) return FA_ERR_INVALID_ARGUMENT;
-  const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
+  const fa_status st = fa::validate(B, H_q, H_kv, N, d, scale, causal);
   if (st != FA_OK) return st;
   if (d != 128) return FA_ERR_UNSUPPORTED;
   for (float f : {q_descale, k_descale, v_descale})
@@ -229,7 +217,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       int H_q, int H_kv, int N, int d, float scale, int causal,
                       cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
-  const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
+  const fa_status st = fa::validate(B, H_q, H_kv, N, d, scale, causal);
   if (st != FA_OK) return st;
   if (d == 256) return FA_ERR_UNSUPPORTED;  // forward only
   const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
@@ -275,7 +263,7 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
                                     void* dv, int B, int H_q, int H_kv, int N, int d, float scale,
                                     int causal, cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
-  const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
+  const fa_status st = fa::validate(B, H_q, H_kv, N, d, scale, causal);
   if (st != FA_OK) return st;
   if (d == 256) return FA_ERR_UNSUPPORTED;  // forward only
   const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
@@ -339,7 +327,7 @@ fa_status fa_set_forward_tile_rows(int rows) {
 
 int fa_forward_tile_rows_for(int B, int H_q, int H_kv, int N_q, int N_kv, int d, int causal,
                              int q_offset, int sms) {
-  if (validate(B, H_q, H_kv, N_q, d, 1.0f, causal) != FA_OK) return 0;
+  if (fa::validate(B, H_q, H_kv, N_q, d, 1.0f, causal) != FA_OK) return 0;
   if (N_kv < 1 || q_offset < 0 || sms < 1) return 0;
   fa::AttnShape s{B, H_q, H_kv, N_q, d, 1.0f, causal};
   s.Nk = N_kv;

@@ -8,7 +8,11 @@
 #include <atomic>
 
 #include <cstdint>
+#include <mutex>
 #include <utility>
+#include <vector>
+
+#include "fa.h"
 
 namespace fa {
 
@@ -86,6 +90,38 @@ inline long long heads_per_group(long long keys, int d, double elem_bytes, int G
   if (kv_heads < 1) kv_heads = 1;
   const long long hpg = kv_heads * G;
   return hpg < n_heads ? hpg : n_heads;
+}
+
+// Checks the sizes, scale and causal flag shared by every attention entry
+// point: B, H_q, H_kv, N >= 1, H_q % H_kv == 0, scale finite and > 0, causal
+// 0 or 1, B*H_q*N*d < 2^40 and at most 65535 query tiles per head
+// (FA_ERR_INVALID_ARGUMENT); d in {64, 96, 128, 256} (else FA_ERR_UNSUPPORTED).
+// Entry points that support fewer head dimensions check that afterwards.
+fa_status validate(int B, int H_q, int H_kv, int N, int d, float scale, int causal);
+
+// The device address of a __device__ variable on the current device, looked
+// up with cudaGetSymbolAddress once per device and cached (the host-side name
+// of such a variable is a stand-in, never the device memory).  The cache has
+// one slot per device the process sees.  nullptr if a CUDA call fails.
+template <typename T>
+void* symbol_address_cached(const T& symbol) {
+  static std::mutex mu;
+  static std::vector<void*> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.empty()) {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || n < 1) return nullptr;
+    cache.assign(static_cast<size_t>(n), nullptr);
+  }
+  if (static_cast<size_t>(dev) >= cache.size()) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+    cache[dev] = p;
+  }
+  return cache[dev];
 }
 
 // Query rows per CTA for the forward: 0 = chosen per shape, 128 or 256.

@@ -29,22 +29,10 @@ namespace {
 // followed by the fp32 dQ accumulator.  Shared by every call on a device.
 static __device__ __align__(256) unsigned char fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
-// Device address of fa_noalloc_scratch, looked up once per device.  In host
-// code the array's name stands for a host-side shadow, never for the device
-// memory itself, so kernels must be given this address instead.
-void* scratch_address() {
-  static void* cache[64] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, fa_noalloc_scratch) != cudaSuccess) return nullptr;
-    cache[dev] = p;
-  }
-  return cache[dev];
-}
+// Device address of fa_noalloc_scratch on the current device, looked up once
+// per device.  In host code the array's name stands for a host-side shadow,
+// never for the device memory itself, so kernels must be given this address.
+void* scratch_address() { return fa::symbol_address_cached(fa_noalloc_scratch); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -56,11 +44,10 @@ extern "C" fa_status fa_backward_noalloc(const void* q, const void* k, const voi
                                          int N, int d, float scale, int causal,
                                          cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
-  if (B < 1 || H_q < 1 || H_kv < 1 || N < 1 || H_q % H_kv != 0) return FA_ERR_INVALID_ARGUMENT;
-  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARGUMENT;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARGUMENT;
-  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
-  if ((N + 127) / 128 > 65535) return FA_ERR_INVALID_ARGUMENT;
+  // The checks of fa_backward, in the same order, so both return the same codes.
+  const fa_status st = fa::validate(B, H_q, H_kv, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
   const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void* p : p16)
     if (!aligned16(p)) return FA_ERR_INVALID_ARGUMENT;

@@ -8,7 +8,8 @@ import pytest
 import torch
 
 import oracle
-from parity import check_forward, forward_vs_oracle, gpu_forward
+from parity import (check_forward, forward_every_element, forward_vs_oracle, gpu_forward,
+                    nan_forward, nan_outputs)
 from workloads import WORKLOADS, as_f64, make_inputs, workload_inputs
 
 pytestmark = pytest.mark.gpu
@@ -78,7 +79,7 @@ def test_head_dim_96_query_offset():
     inp = make_inputs(2, 4, 1, 200, 96, seed=960, Nk=713)
     scale = 1.0 / math.sqrt(96)
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    o, lse = fa.attention_forward(q, k, v, causal=True, scale=scale, q_offset=513)
+    o, lse = nan_forward(q, k, v, causal=True, scale=scale, q_offset=513)
     torch.cuda.synchronize()
     assert fa.fa_last_device_error() == 0
     o_ref, l_ref = oracle.attention_forward(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]),
@@ -108,7 +109,7 @@ def test_head_dim_256_query_offset(Nq, Nk, off, causal):
     inp = make_inputs(1, 4, 2, Nq, 256, seed=Nq + Nk + 256, Nk=Nk)
     scale = 1.0 / math.sqrt(256)
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    o, lse = fa.attention_forward(q, k, v, causal=causal, scale=scale, q_offset=off)
+    o, lse = nan_forward(q, k, v, causal=causal, scale=scale, q_offset=off)
     torch.cuda.synchronize()
     assert fa.fa_last_device_error() == 0
     o_ref, l_ref = oracle.attention_forward(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]),
@@ -135,23 +136,63 @@ def test_causal_n4096_d64_full():
     forward_vs_oracle(workload_inputs(w), w.causal, w.scale)
 
 
-def _sampled(w, n_rows, seed):
-    rng = np.random.default_rng(seed)
-    rows = np.unique(np.concatenate([[0, 1, 127, 128, w.N - 1],
-                                     rng.integers(0, w.N, n_rows)]))
-    return rows
-
-
-@pytest.mark.parametrize("name", ["causal_n8192_d128", "causal_gqa_n16384_d128",
-                                  "causal_n8192_d96", "causal_n8192_d256",
-                                  "causal_gqa_n16384_d256"])
-def test_full_size_sampled_rows(name):
-    """Full-size workloads in the benchmark's launch configuration: every head,
-    a seeded sample of query rows plus the tile edges, against the oracle."""
+@pytest.mark.parametrize("name", ["causal_n8192_d128", "causal_gqa_n16384_d128"])
+def test_full_size_every_element(name):
+    """The two d = 128 forward targets (B4 H16 N8192 and GQA B1 Hq32 Hkv8
+    N16384) at full size, in the launch configuration the benchmark times
+    (per-shape tile size, launch order and head grouping), into NaN-filled
+    outputs: every element of O and L against the oracle, which is evaluated
+    in blocks of query rows."""
+    import exact_attention_27_gb300 as fa
     w = WORKLOADS[name]
     inp = workload_inputs(w)
-    rows = _sampled(w, 24, seed=3)
-    (_, _, _), (o, lse) = forward_vs_oracle(inp, w.causal, w.scale, rows=rows)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o, lse = nan_outputs(q)
+    fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == 0
+    del q, k, v
+    forward_every_element(inp, w.causal, w.scale, o, lse, what=name)
+
+
+def _tile_rows(N, seed):
+    """The first and last row of every 128-row query tile, plus one row at a
+    seeded offset inside each tile."""
+    rng = np.random.default_rng(seed)
+    starts = np.arange(0, N, 128)
+    ends = np.minimum(starts + 127, N - 1)
+    inner = np.minimum(starts + rng.integers(1, 127, starts.size), N - 1)
+    return np.unique(np.concatenate([starts, ends, inner]))
+
+
+@pytest.mark.parametrize("name", ["causal_n8192_d96", "causal_n8192_d256",
+                                  "causal_gqa_n16384_d256"])
+def test_full_size_every_tile_and_two_whole_heads(name):
+    """Full-size d = 96 and d = 256 workloads in the benchmark's launch
+    configuration, into NaN-filled outputs: every element finite (so written),
+    three rows of every 128-row query tile of every head against the oracle,
+    and every row of two whole heads (the first head of the first batch and
+    the last head of the last batch)."""
+    import exact_attention_27_gb300 as fa
+    w = WORKLOADS[name]
+    inp = workload_inputs(w)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o, lse = nan_outputs(q)
+    fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == 0
+    del q, k, v
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    rows = _tile_rows(w.N, seed=w.d)
+    o_ref, l_ref = oracle.attention_forward(as_f64(inp["q"]), as_f64(inp["k"]),
+                                            as_f64(inp["v"]), w.scale, w.causal, rows=rows)
+    check_forward(o[:, :, rows], lse[:, :, rows], o_ref, l_ref, f"{name} tile rows")
+    G = w.Hq // w.Hkv
+    for b, h in ((0, 0), (w.B - 1, w.Hq - 1)):
+        head = {"q": inp["q"][b:b + 1, h:h + 1], "k": inp["k"][b:b + 1, h // G:h // G + 1],
+                "v": inp["v"][b:b + 1, h // G:h // G + 1]}
+        forward_every_element(head, w.causal, w.scale, o[b:b + 1, h:h + 1],
+                              lse[b:b + 1, h:h + 1], block_rows=512, what=f"{name} head {b},{h}")
 
 
 def test_deterministic():
@@ -186,7 +227,7 @@ def test_query_offset_against_the_oracle(Nq, Nk, off, causal, d, Hq, Hkv):
     inp = make_inputs(1, Hq, Hkv, Nq, d, seed=Nq + Nk, Nk=Nk)
     scale = 1.0 / math.sqrt(d)
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    o, lse = fa.attention_forward(q, k, v, causal=causal, scale=scale, q_offset=off)
+    o, lse = nan_forward(q, k, v, causal=causal, scale=scale, q_offset=off)
     torch.cuda.synchronize()
     assert fa.fa_last_device_error() == 0
     o_ref, l_ref = oracle.attention_forward(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]),
@@ -200,10 +241,10 @@ def test_offset_rows_equal_rows_of_the_full_forward():
     import exact_attention_27_gb300 as fa
     inp = make_inputs(2, 4, 2, 700, 64, seed=77)
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    o_full, l_full = fa.attention_forward(q, k, v, causal=True, scale=0.125)
+    o_full, l_full = nan_forward(q, k, v, causal=True, scale=0.125)
     for off, n in ((0, 128), (100, 300), (699, 1), (513, 187)):
         qs = q[:, :, off:off + n].contiguous()
-        o, lse = fa.attention_forward(qs, k, v, causal=True, scale=0.125, q_offset=off)
+        o, lse = nan_forward(qs, k, v, causal=True, scale=0.125, q_offset=off)
         torch.cuda.synchronize()
         assert torch.equal(o, o_full[:, :, off:off + n]), off
         assert torch.equal(lse, l_full[:, :, off:off + n]), off
@@ -213,8 +254,8 @@ def test_forward_ex_with_equal_lengths_is_forward():
     import exact_attention_27_gb300 as fa
     inp = make_inputs(1, 2, 2, 333, 128, seed=4)
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    o1, l1 = fa.attention_forward(q, k, v, causal=True)
-    o2, l2 = fa.attention_forward(q, k, v, causal=True, q_offset=0)
+    o1, l1 = nan_forward(q, k, v, causal=True)
+    o2, l2 = nan_forward(q, k, v, causal=True, q_offset=0)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
@@ -246,7 +287,7 @@ def test_both_tile_sizes_with_query_offset(tile_rows, rows, d):
     tile_rows(rows)
     inp = make_inputs(1, 4, 2, 300, d, seed=31, Nk=941)
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    o, lse = fa.attention_forward(q, k, v, causal=True, scale=0.1, q_offset=641)
+    o, lse = nan_forward(q, k, v, causal=True, scale=0.1, q_offset=641)
     torch.cuda.synchronize()
     o_ref, l_ref = oracle.attention_forward(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]),
                                             0.1, True, q_offset=641)

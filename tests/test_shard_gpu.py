@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from exact_attention_27_gb300 import shard
-from parity import check_grads
+from parity import check_grads, nan_backward, nan_forward
 from workloads import make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -27,11 +27,11 @@ def test_shard_launches_match_full_launch(B, Hq, Hkv, N, d):
     import exact_attention_27_gb300 as fa
     scale = 1.0 / math.sqrt(d)
     inp = {n: t.cuda() for n, t in make_inputs(B, Hq, Hkv, N, d, seed=3, with_grad=True).items()}
-    o, lse = fa.attention_forward(inp["q"], inp["k"], inp["v"], causal=True, scale=scale)
-    dq, dk, dv = fa.attention_backward(inp["q"], inp["k"], inp["v"], o, lse, inp["do"],
-                                       causal=True, scale=scale)
-    outs = {"o": torch.empty_like(o), "lse": torch.empty_like(lse), "dq": torch.empty_like(dq),
-            "dk": torch.empty_like(dk), "dv": torch.empty_like(dv)}
+    o, lse = nan_forward(inp["q"], inp["k"], inp["v"], causal=True, scale=scale)
+    dq, dk, dv = nan_backward(inp["q"], inp["k"], inp["v"], o, lse, inp["do"],
+                              causal=True, scale=scale)
+    outs = {n: torch.full_like(t, float("nan"))
+            for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
     world = 2
     for rank in range(world):
         views, (Bs, Hqs, Hkvs) = shard.shard(dict(inp, **outs), Hq, Hkv, rank, world)
