@@ -582,11 +582,12 @@ GRAPH_FWD_WORKLOAD = "causal_n4096_d64"
 BWD_WORKLOADS = [
     ("causal bwd B2 H16 N4096 d128 bf16", (2, 16, 16, 4096, 128), False),
     ("causal bwd B2 H16 N4096 d96 bf16", (2, 16, 16, 4096, 96), False),
+    ("causal bwd B2 H16 N4096 d256 bf16", (2, 16, 16, 4096, 256), False),
     ("causal bwd B2 H8 N4096 d64 bf16, deterministic", (2, 8, 8, 4096, 64), True),
 ]
 # Short names for --backward-only.
 BWD_NAMES = {"causal_bwd_n4096_d128": 0, "causal_bwd_n4096_d96": 1,
-             "causal_bwd_det_n4096_d64": 2}
+             "causal_bwd_n4096_d256": 2, "causal_bwd_det_n4096_d64": 3}
 
 
 def backward_workloads(fa, torch, tflops_peak, peak_src):

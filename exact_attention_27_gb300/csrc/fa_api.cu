@@ -95,6 +95,67 @@ namespace fa {
 
 uint32_t* device_error_word() { return error_word(); }
 
+fa_status validate_backward(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dO, const void* dq, const void* dk,
+                            const void* dv, int B, int H_q, int H_kv, int N, int d, float scale,
+                            int causal) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
+  const fa_status st = validate(B, H_q, H_kv, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
+  for (const void* p : p16)
+    if (!aligned16(p)) return FA_ERR_INVALID_ARGUMENT;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_INVALID_ARGUMENT;
+  return FA_OK;
+}
+
+bool backward_uses_two_kernels(int d, bool deterministic) { return deterministic || d == 256; }
+
+size_t backward_scratch_bytes(int B, int H_q, int N, int d, bool deterministic,
+                              size_t* acc_off) {
+  const size_t rows = static_cast<size_t>(B) * H_q * N;
+  const size_t d_bytes = rows * sizeof(float);
+  if (backward_uses_two_kernels(d, deterministic)) {
+    *acc_off = 0;
+    return d_bytes;
+  }
+  *acc_off = (d_bytes + 1023) & ~static_cast<size_t>(1023);  // accumulator 1 KiB aligned
+  return *acc_off + rows * d * sizeof(float);
+}
+
+fa_status enqueue_backward(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                           const AttnShape& s, float* Dbuf, float* acc, bool deterministic,
+                           bool timed, cudaStream_t stream) {
+  uint32_t* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  const int d = s.d, N = s.N;
+  const long long rows = static_cast<long long>(s.B) * s.Hq * N;
+  const long long qplanes = static_cast<long long>(s.B) * s.Hq;
+  const long long kvplanes = static_cast<long long>(s.B) * s.Hkv;
+  const bool two = backward_uses_two_kernels(d, deterministic);
+  if (!two && !acc) return FA_ERR_INVALID_ARGUMENT;
+  BwdMaps m{};
+  bool ok = make_map_bf16(&m.q, q, d, N, qplanes) && make_kv_map_bf16(&m.k, k, d, N, kvplanes) &&
+            make_kv_map_bf16(&m.v, v, d, N, kvplanes) && make_map_bf16(&m.dO, dO, d, N, qplanes);
+  if (ok && !two)
+    ok = encode_map_f32_acc(&m.dq_acc, acc, d, N, qplanes) &&
+         encode_map_f32_acc32(&m.dq_acc32, acc, d, N, qplanes);
+  if (!ok) return FA_ERR_CUDA;
+  // Main dK/dV kernel between the caller's timing events, if any.
+  timed = timed && g_bwd_before && g_bwd_after;
+  cudaError_t e = launch_preprocess(o, dO, Dbuf, rows, d, stream, two ? nullptr : acc);
+  if (e == cudaSuccess && timed) e = cudaEventRecord(g_bwd_before, stream);
+  if (e == cudaSuccess)
+    e = d == 256 ? launch_backward_d256_kv(m, lse, Dbuf, dk, dv, s, err, stream)
+                 : launch_backward(m, lse, Dbuf, acc, dk, dv, s, err, stream, !two);
+  if (e == cudaSuccess && timed) e = cudaEventRecord(g_bwd_after, stream);
+  if (e == cudaSuccess)
+    e = two ? launch_backward_dq(m, lse, Dbuf, dq, s, err, stream)
+            : launch_dq_finalize(acc, dq, rows * d, s.scale, stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status validate(int B, int H_q, int H_kv, int N, int d, float scale, int causal) {
   if (B < 1 || H_q < 1 || H_kv < 1 || N < 1) return FA_ERR_INVALID_ARGUMENT;
   if (H_q % H_kv != 0) return FA_ERR_INVALID_ARGUMENT;
@@ -206,7 +267,7 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o,
 fa_status fa_backward_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
                                  cudaStream_t stream) {
   if (!o || !dO || !D || rows < 1) return FA_ERR_INVALID_ARGUMENT;
-  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (!aligned16(o) || !aligned16(dO) || (reinterpret_cast<uintptr_t>(D) & 3u))
     return FA_ERR_INVALID_ARGUMENT;
   return fa::launch_preprocess(o, dO, D, rows, d, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -216,80 +277,39 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
                       int H_q, int H_kv, int N, int d, float scale, int causal,
                       cudaStream_t stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
-  const fa_status st = fa::validate(B, H_q, H_kv, N, d, scale, causal);
+  const fa_status st = fa::validate_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H_q, H_kv, N, d,
+                                             scale, causal);
   if (st != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;  // forward only
-  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
-  for (const void* p : p16)
-    if (!aligned16(p)) return FA_ERR_INVALID_ARGUMENT;
-  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_INVALID_ARGUMENT;
-  uint32_t* err = error_word();
-  if (!err) return FA_ERR_CUDA;
-
-  const long long rows = static_cast<long long>(B) * H_q * N;
-  const size_t d_bytes = static_cast<size_t>(rows) * sizeof(float);
-  const size_t acc_bytes = static_cast<size_t>(rows) * d * sizeof(float);
+  size_t acc_off = 0;
+  const size_t bytes = fa::backward_scratch_bytes(B, H_q, N, d, false, &acc_off);
   void* scratch = nullptr;
-  // D first, then the dQ accumulator (offset rounded up to 1 KB).
-  const size_t acc_off = (d_bytes + 1023) & ~static_cast<size_t>(1023);
-  if (cudaMallocAsync(&scratch, acc_off + acc_bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMallocAsync(&scratch, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
   float* Dbuf = static_cast<float*>(scratch);
-  float* acc = reinterpret_cast<float*>(static_cast<char*>(scratch) + acc_off);
-
-  fa::BwdMaps m;
-  bool ok = make_map_bf16(&m.q, q, d, N, static_cast<long long>(B) * H_q) &&
-            make_map_bf16(&m.k, k, d, N, static_cast<long long>(B) * H_kv) &&
-            make_map_bf16(&m.v, v, d, N, static_cast<long long>(B) * H_kv) &&
-            make_map_bf16(&m.dO, dO, d, N, static_cast<long long>(B) * H_q) &&
-            make_map(&m.dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, d, N,
-                     static_cast<long long>(B) * H_q, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            make_map(&m.dq_acc32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, acc, d, N,
-                     static_cast<long long>(B) * H_q, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  float* acc = acc_off ? reinterpret_cast<float*>(static_cast<char*>(scratch) + acc_off) : nullptr;
   fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
-  cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
-  if (e == cudaSuccess) e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream, acc);
-  const bool timed = g_bwd_before && g_bwd_after;
-  if (e == cudaSuccess && timed) e = cudaEventRecord(g_bwd_before, stream);
-  if (e == cudaSuccess) e = fa::launch_backward(m, lse, Dbuf, acc, dk, dv, s, err, stream);
-  if (e == cudaSuccess && timed) e = cudaEventRecord(g_bwd_after, stream);
-  if (e == cudaSuccess) e = fa::launch_dq_finalize(acc, dq, rows * d, scale, stream);
+  const fa_status r = fa::enqueue_backward(q, k, v, o, lse, dO, dq, dk, dv, s, Dbuf, acc,
+                                           /*deterministic=*/false, /*timed=*/true, stream);
   const cudaError_t ef = cudaFreeAsync(scratch, stream);
-  return (e == cudaSuccess && ef == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
+  return r != FA_OK ? r : (ef == cudaSuccess ? FA_OK : FA_ERR_CUDA);
 }
 
 fa_status fa_backward_deterministic(const void* q, const void* k, const void* v, const void* o,
                                     const float* lse, const void* dO, void* dq, void* dk,
                                     void* dv, int B, int H_q, int H_kv, int N, int d, float scale,
                                     int causal, cudaStream_t stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
-  const fa_status st = fa::validate(B, H_q, H_kv, N, d, scale, causal);
+  const fa_status st = fa::validate_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H_q, H_kv, N, d,
+                                             scale, causal);
   if (st != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;  // forward only
-  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
-  for (const void* p : p16)
-    if (!aligned16(p)) return FA_ERR_INVALID_ARGUMENT;
-  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_INVALID_ARGUMENT;
-  uint32_t* err = error_word();
-  if (!err) return FA_ERR_CUDA;
-  const long long rows = static_cast<long long>(B) * H_q * N;
+  size_t acc_off = 0;
+  const size_t bytes = fa::backward_scratch_bytes(B, H_q, N, d, true, &acc_off);
   void* scratch = nullptr;
-  if (cudaMallocAsync(&scratch, static_cast<size_t>(rows) * sizeof(float), stream) != cudaSuccess)
-    return FA_ERR_CUDA;
-  float* Dbuf = static_cast<float*>(scratch);
-  fa::BwdMaps m{};
-  const bool ok = make_map_bf16(&m.q, q, d, N, static_cast<long long>(B) * H_q) &&
-                  make_map_bf16(&m.k, k, d, N, static_cast<long long>(B) * H_kv) &&
-                  make_map_bf16(&m.v, v, d, N, static_cast<long long>(B) * H_kv) &&
-                  make_map_bf16(&m.dO, dO, d, N, static_cast<long long>(B) * H_q);
+  if (cudaMallocAsync(&scratch, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
   fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
-  cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
-  if (e == cudaSuccess) e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream);
-  if (e == cudaSuccess)
-    e = fa::launch_backward(m, lse, Dbuf, nullptr, dk, dv, s, err, stream, /*with_dq=*/false);
-  if (e == cudaSuccess) e = fa::launch_backward_dq(m, lse, Dbuf, dq, s, err, stream);
+  const fa_status r = fa::enqueue_backward(q, k, v, o, lse, dO, dq, dk, dv, s,
+                                           static_cast<float*>(scratch), nullptr,
+                                           /*deterministic=*/true, /*timed=*/false, stream);
   const cudaError_t ef = cudaFreeAsync(scratch, stream);
-  return (e == cudaSuccess && ef == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
+  return r != FA_OK ? r : (ef == cudaSuccess ? FA_OK : FA_ERR_CUDA);
 }
 
 const char* fa_status_string(fa_status s) {

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
                                                          const uint4* __restrict__ dO,
                                                          float* __restrict__ out, long long rows,
                                                          float4* __restrict__ dq_acc) {
-  constexpr int PIECES = D / 8;                   // 16-byte pieces per row: 8, 12 or 16
+  constexpr int PIECES = D / 8;                   // 16-byte pieces per row: 8, 12, 16 or 32
   constexpr int TPR = (PIECES % 4 == 0 && PIECES % 8 != 0) ? 4 : PIECES;
   constexpr int VPT = PIECES / TPR;
   static_assert(TPR * VPT == PIECES && (TPR & (TPR - 1)) == 0, "row split");
@@ -635,6 +635,9 @@ cudaError_t launch_preprocess(const void* o, const void* dO, float* Dout, long l
                             acc);
   if (d == 96)
     return launch_dependent(preprocess_kernel<96>, grid, block, 0, stream, o4, dO4, Dout, rows,
+                            acc);
+  if (d == 256)
+    return launch_dependent(preprocess_kernel<256>, grid, block, 0, stream, o4, dO4, Dout, rows,
                             acc);
   return launch_dependent(preprocess_kernel<128>, grid, block, 0, stream, o4, dO4, Dout, rows, acc);
 }

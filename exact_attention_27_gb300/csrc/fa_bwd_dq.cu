@@ -24,10 +24,12 @@
 // reduction is needed (P comes from the saved L), so each query row is split
 // between two warps, 64 key columns each.
 //
-// Warps: 0-7 query rows (warp w: rows 32 (w % 4).., key columns 64 (w / 4)..),
-// 8 TMA producer, 9 MMA issuer and tensor-memory owner.
-// Tensor memory: S buffers [0,128) and [128,256) (dS as bf16 pairs at columns
-// 64g.. over the S columns warp group g read), dP [256,384), dQ [384, 384+DP).
+// Warps: 0-7 query rows (warp w: rows 32 (w % 4).., key columns KH (w / 4)..
+// with KH = BN / 2), 8 TMA producer, 9 MMA issuer and tensor-memory owner.
+// Tensor memory: S buffers [0,BN) and [BN,2BN) (dS as bf16 pairs at columns
+// KH g.. over the S columns warp group g read), dP [2BN,3BN), dQ [COL_DQ,
+// COL_DQ + DP).  Keys come in tiles of BN = 128, or of 64 at D = 256, where
+// the 256-column fp32 dQ leaves room for 64-column S and dP buffers only.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -41,27 +43,31 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Head dimension D in {64, 96, 128}; tiles are DP = D rounded up to a
+// Head dimension D in {64, 96, 128, 256}; tiles are DP = D rounded up to a
 // multiple of 64 columns wide (zero-filled past D), S and dP contract over the
 // D real columns and dQ runs at N = D.
 template <int D>
 struct DqCfg {
   static constexpr int DP = (D + 63) / 64 * 64;  // padded head dimension
   static constexpr int BM = 128;                 // query rows per CTA
-  static constexpr int BN = 128;                 // keys per tile
+  static constexpr int BN = (D == 256) ? 64 : 128;  // keys per tile
+  static constexpr int KH = BN / 2;              // key columns per row warp
   static constexpr int SUB = DP / 64;
-  static constexpr int SUB_BYTES = 128 * 128;
-  static constexpr int TILE = SUB * SUB_BYTES;   // 128 x DP bf16
+  static constexpr int QSUB = 128 * 128;         // 128 query rows x 64 bf16
+  static constexpr int KSUB = BN * 128;          // BN key rows x 64 bf16
+  static constexpr int QTILE = SUB * QSUB;
+  static constexpr int KTILE = SUB * KSUB;
   // K_j is read by S_j and dQ_j, and S_{j+2} is issued right after dQ_j:
   // three K stages let K_{j+2} arrive while K_j and K_{j+1} are in use.
-  // V_j is read by dP_j only.
-  static constexpr int NSK = (D == 64) ? 4 : 3;
-  static constexpr int NSV = (D == 64) ? 4 : 2;
+  // V_j is read by dP_j only.  At D = 256 (64 KB Q and dO tiles) two K
+  // stages and one V stage are what fits.
+  static constexpr int NSK = (D == 64) ? 4 : (D == 256 ? 2 : 3);
+  static constexpr int NSV = (D == 64) ? 4 : (D == 256 ? 1 : 2);
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = OFF_Q + TILE;
-  static constexpr int OFF_K = OFF_DO + TILE;
-  static constexpr int OFF_V = OFF_K + NSK * TILE;
-  static constexpr int OFF_BAR = OFF_V + NSV * TILE;
+  static constexpr int OFF_DO = OFF_Q + QTILE;
+  static constexpr int OFF_K = OFF_DO + QTILE;
+  static constexpr int OFF_V = OFF_K + NSK * KTILE;
+  static constexpr int OFF_BAR = OFF_V + NSV * KTILE;
   static constexpr int B_QD = 0;
   static constexpr int B_KFULL = 1;                // [NSK]
   static constexpr int B_KEMPTY = B_KFULL + NSK;   // [NSK]
@@ -78,7 +84,8 @@ struct DqCfg {
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0, COL_DP = 256, COL_DQ = 384;  // S buffer b at COL_S + 128 b
+  static constexpr uint32_t COL_S = 0, COL_DP = 2 * BN;  // S buffer b at COL_S + BN b
+  static constexpr uint32_t COL_DQ = (D == 256) ? 256 : 384;
   static_assert(COL_DQ + DP <= TMEM_COLS, "tensor memory");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -120,7 +127,9 @@ __global__ void __launch_bounds__(320, 1)
   const int b = bh / p.Hq;
   const int hq = bh - b * p.Hq;
   const int kvz = b * (p.Hq / p.G) + hq / p.G;
-  const int n_kv = CAUSAL ? min(qt + 1, p.n_ktiles) : p.n_ktiles;
+  // Under the causal mask the tile's last row qt BM + BM - 1 sees key tiles
+  // up to the one holding that position.
+  const int n_kv = CAUSAL ? min((qt * C::BM + C::BM - 1) / C::BN + 1, p.n_ktiles) : p.n_ktiles;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_QD), 1);
@@ -164,11 +173,11 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(bar(C::B_QD), 2 * C::TILE);
+      mbar_arrive_expect_tx(bar(C::B_QD), 2 * C::QTILE);
 #pragma unroll
       for (int s = 0; s < C::SUB; ++s) {
-        tma_load_3d(sQ + s * C::SUB_BYTES, &tmQ, bar(C::B_QD), 64 * s, qt * C::BM, bh);
-        tma_load_3d(sdO + s * C::SUB_BYTES, &tmdO, bar(C::B_QD), 64 * s, qt * C::BM, bh);
+        tma_load_3d(sQ + s * C::QSUB, &tmQ, bar(C::B_QD), 64 * s, qt * C::BM, bh);
+        tma_load_3d(sdO + s * C::QSUB, &tmdO, bar(C::B_QD), 64 * s, qt * C::BM, bh);
       }
       // K_j then V_j, in the order the products need them (S_j comes before dP_j).
       int k_issued = 0, v_issued = 0;
@@ -177,20 +186,20 @@ __global__ void __launch_bounds__(320, 1)
         if (j >= C::NSK && !mbar_wait(bar(C::B_KEMPTY + sk), ((j / C::NSK) - 1) & 1, abort_flag,
                                       p.err, kErrTimeoutLoad))
           break;
-        mbar_arrive_expect_tx(bar(C::B_KFULL + sk), C::TILE);
+        mbar_arrive_expect_tx(bar(C::B_KFULL + sk), C::KTILE);
 #pragma unroll
         for (int s = 0; s < C::SUB; ++s)
-          tma_load_3d(sK + sk * C::TILE + s * C::SUB_BYTES, &tmK, bar(C::B_KFULL + sk), 64 * s,
+          tma_load_3d(sK + sk * C::KTILE + s * C::KSUB, &tmK, bar(C::B_KFULL + sk), 64 * s,
                       j * C::BN, kvz);
         k_issued = j + 1;
         const int sv = j % C::NSV;
         if (j >= C::NSV && !mbar_wait(bar(C::B_VEMPTY + sv), ((j / C::NSV) - 1) & 1, abort_flag,
                                       p.err, kErrTimeoutLoad))
           break;
-        mbar_arrive_expect_tx(bar(C::B_VFULL + sv), C::TILE);
+        mbar_arrive_expect_tx(bar(C::B_VFULL + sv), C::KTILE);
 #pragma unroll
         for (int s = 0; s < C::SUB; ++s)
-          tma_load_3d(sV + sv * C::TILE + s * C::SUB_BYTES, &tmV, bar(C::B_VFULL + sv), 64 * s,
+          tma_load_3d(sV + sv * C::KTILE + s * C::KSUB, &tmV, bar(C::B_VFULL + sv), 64 * s,
                       j * C::BN, kvz);
         v_issued = j + 1;
       }
@@ -206,13 +215,13 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
-      constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);  // S, dP
+      constexpr uint32_t ID_S = idesc_bf16_f32(128, C::BN, false, false);  // S, dP
       constexpr uint32_t ID_Q = idesc_bf16_f32(128, D, false, true);  // dQ (B = K MN-major), N = D
       const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t do_desc = smem_desc_sw128(sdO, 16, 1024);
       const uint64_t k_kmaj = smem_desc_sw128(sK, 16, 1024);
       const uint64_t v_kmaj = smem_desc_sw128(sV, 16, 1024);
-      const uint64_t k_mn = smem_desc_sw128(sK, C::SUB_BYTES, 1024);
+      const uint64_t k_mn = smem_desc_sw128(sK, C::KSUB, 1024);
       bool ok = mbar_wait(bar(C::B_QD), 0, abort_flag, p.err, kErrTimeoutMma);
       // S_j = Q K_j^T into S buffer j % 2.
       auto issue_s = [&](int j) -> bool {
@@ -220,14 +229,13 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait(bar(C::B_KFULL + sk), (j / C::NSK) & 1, abort_flag, p.err, kErrTimeoutMma))
           return false;
         tc_fence_after();
-        const uint32_t dst = tmem + C::COL_S + 128 * (j & 1);
-        const uint64_t kd = desc_add(k_kmaj, sk * C::TILE);
+        const uint32_t dst = tmem + C::COL_S + C::BN * (j & 1);
+        const uint64_t kd = desc_add(k_kmaj, sk * C::KTILE);
         mma_ss_k<ID_S, 0>(dst, q_desc, kd);
 #pragma unroll
-        for (int kk = 1; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          mma_ss_k<ID_S, 1>(dst, desc_add(q_desc, off), desc_add(kd, off));
-        }
+        for (int kk = 1; kk < D / 16; ++kk)
+          mma_ss_k<ID_S, 1>(dst, desc_add(q_desc, (kk >> 2) * C::QSUB + (kk & 3) * 32),
+                            desc_add(kd, (kk >> 2) * C::KSUB + (kk & 3) * 32));
         mma_commit(bar(C::B_SFULL + (j & 1)));
         return true;
       };
@@ -237,13 +245,13 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait(bar(C::B_VFULL + sv), (j / C::NSV) & 1, abort_flag, p.err, kErrTimeoutMma))
           return false;
         tc_fence_after();
-        const uint64_t vd = desc_add(v_kmaj, sv * C::TILE);
+        const uint64_t vd = desc_add(v_kmaj, sv * C::KTILE);
         mma_ss_k<ID_S, 0>(tmem + C::COL_DP, do_desc, vd);
 #pragma unroll
-        for (int kk = 1; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
-          mma_ss_k<ID_S, 1>(tmem + C::COL_DP, desc_add(do_desc, off), desc_add(vd, off));
-        }
+        for (int kk = 1; kk < D / 16; ++kk)
+          mma_ss_k<ID_S, 1>(tmem + C::COL_DP,
+                            desc_add(do_desc, (kk >> 2) * C::QSUB + (kk & 3) * 32),
+                            desc_add(vd, (kk >> 2) * C::KSUB + (kk & 3) * 32));
         mma_commit(bar(C::B_DPFULL));
         mma_commit(bar(C::B_VEMPTY + sv));
         return true;
@@ -262,19 +270,20 @@ __global__ void __launch_bounds__(320, 1)
                        kErrTimeoutMma))
           break;
         tc_fence_after();
-        // dQ += dS_j K_j.  dS of keys 64g.. sits packed (bf16 pairs) at
-        // columns 64g.. of the S buffer, 16 keys = 8 columns per step; K_j is
-        // read MN-major, 16 key rows (2 KB) per step.
+        // dQ += dS_j K_j.  dS of keys KH g.. sits packed (bf16 pairs) at
+        // columns KH g.. of the S buffer, 16 keys = 8 columns per step; K_j
+        // is read MN-major, 16 key rows (2 KB) per step.
         const int sk = j % C::NSK;
-        const uint32_t sb = tmem + C::COL_S + 128 * (j & 1);
-        const uint64_t kmn = desc_add(k_mn, sk * C::TILE);
+        const uint32_t sb = tmem + C::COL_S + C::BN * (j & 1);
+        const uint64_t kmn = desc_add(k_mn, sk * C::KTILE);
+        constexpr int KPW = C::KH / 16;  // 16-key steps per row warp's columns
         if (j == 0)
           mma_ts_k<ID_Q, 0>(tmem + C::COL_DQ, sb, kmn);
         else
           mma_ts_k<ID_Q, 1>(tmem + C::COL_DQ, sb, kmn);
 #pragma unroll
-        for (int kk = 1; kk < 8; ++kk)
-          mma_ts_k<ID_Q, 1>(tmem + C::COL_DQ, sb + (kk >> 2) * 64 + (kk & 3) * 8,
+        for (int kk = 1; kk < C::BN / 16; ++kk)
+          mma_ts_k<ID_Q, 1>(tmem + C::COL_DQ, sb + (kk / KPW) * C::KH + (kk % KPW) * 8,
                             desc_add(kmn, kk * 2048));
         mma_commit(bar(C::B_KEMPTY + sk));
         // S_{j+2} reuses this S buffer; the products run in issue order, so it
@@ -314,21 +323,23 @@ __global__ void __launch_bounds__(320, 1)
                                                kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t scol = C::COL_S + 128 * (j & 1) + 64 * g;
-      uint32_t sv[64], dpv[64];
-      tmem_ld32(tmem + lane_off + scol, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(tmem + lane_off + scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld32(tmem + lane_off + C::COL_DP + 64 * g, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
-      tmem_ld32(tmem + lane_off + C::COL_DP + 64 * g + 32,
-                *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
+      const uint32_t scol = C::COL_S + C::BN * (j & 1) + C::KH * g;
+      constexpr int KH = C::KH;
+      uint32_t sv[KH], dpv[KH];
+#pragma unroll
+      for (int c = 0; c < KH / 32; ++c) {
+        tmem_ld32(tmem + lane_off + scol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
+        tmem_ld32(tmem + lane_off + C::COL_DP + KH * g + 32 * c,
+                  *reinterpret_cast<uint32_t(*)[32]>(&dpv[32 * c]));
+      }
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive_warp(bar(C::B_DPFREE));
-      const int kbase = j * C::BN + 64 * g;
-      const bool need_mask = (kbase + 64 > p.N) || (CAUSAL && kbase + 63 > qt * C::BM);
-      uint32_t pk[32];
+      const int kbase = j * C::BN + KH * g;
+      const bool need_mask = (kbase + KH > p.N) || (CAUSAL && kbase + KH - 1 > qt * C::BM);
+      uint32_t pk[KH / 2];
 #pragma unroll
-      for (int u = 0; u < 32; ++u) {
+      for (int u = 0; u < KH / 2; ++u) {
         float p0, p1;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * u]), __uint_as_float(sv[2 * u + 1])),
                          c2, nl2),
@@ -347,7 +358,10 @@ __global__ void __launch_bounds__(320, 1)
         pk[u] = pack_bf16x2(d0, d1);
       }
       // dS (bf16 pairs) over S columns this warp has already read.
-      tmem_st32(tmem + lane_off + scol, pk);
+      if constexpr (KH == 64)
+        tmem_st32(tmem + lane_off + scol, pk);
+      else
+        tmem_st16(tmem + lane_off + scol, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(bar(C::B_DSREADY + (j & 1)));
@@ -428,6 +442,9 @@ cudaError_t launch_backward_dq(const BwdMaps& m, const float* lse, const float* 
   if (s.d == 96)
     return s.causal ? launch_dq_t<96, true>(m, lse, Dv, dq, s, err, stream)
                     : launch_dq_t<96, false>(m, lse, Dv, dq, s, err, stream);
+  if (s.d == 256)
+    return s.causal ? launch_dq_t<256, true>(m, lse, Dv, dq, s, err, stream)
+                    : launch_dq_t<256, false>(m, lse, Dv, dq, s, err, stream);
   return s.causal ? launch_dq_t<128, true>(m, lse, Dv, dq, s, err, stream)
                   : launch_dq_t<128, false>(m, lse, Dv, dq, s, err, stream);
 }

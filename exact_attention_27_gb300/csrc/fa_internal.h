@@ -99,6 +99,34 @@ inline long long heads_per_group(long long keys, int d, double elem_bytes, int G
 // Entry points that support fewer head dimensions check that afterwards.
 fa_status validate(int B, int H_q, int H_kv, int N, int d, float scale, int causal);
 
+// validate() plus the pointer checks of the backward entry points: every
+// pointer non-null, 16-byte aligned (lse 4-byte aligned).
+fa_status validate_backward(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dO, const void* dq, const void* dk,
+                            const void* dv, int B, int H_q, int H_kv, int N, int d, float scale,
+                            int causal);
+
+// Whether the backward of head dimension d runs as two kernels (dK/dV, then
+// dQ walking the key tiles in order; no dQ accumulator): always when
+// `deterministic`, and at d = 256, whose only backward this is.
+bool backward_uses_two_kernels(int d, bool deterministic);
+
+// Scratch of one backward call: D (B*H_q*N fp32) and, for the single-kernel
+// path, the fp32 dQ accumulator at byte offset *acc_off (1 KiB aligned);
+// *acc_off = 0 when there is none.  Returns the total in bytes.
+size_t backward_scratch_bytes(int B, int H_q, int N, int d, bool deterministic,
+                              size_t* acc_off);
+
+// Enqueues a validated backward pass on `stream`, given its scratch: Dbuf
+// (B*H_q*N floats) and, unless the call runs as two kernels, acc (the fp32
+// dQ accumulator, B*H_q*N*d floats, 16-byte aligned; its previous contents
+// do not matter, the row-dot pass clears it).  `timed` records the events set
+// by fa_set_backward_events around the main dK/dV kernel.
+fa_status enqueue_backward(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                           const AttnShape& s, float* Dbuf, float* acc, bool deterministic,
+                           bool timed, cudaStream_t stream);
+
 // The device address of a __device__ variable on the current device, looked
 // up with cudaGetSymbolAddress once per device and cached (the host-side name
 // of such a variable is a stand-in, never the device memory).  The cache has
@@ -138,7 +166,7 @@ cudaError_t launch_preprocess(const void* o, const void* dO, float* D, long long
                               cudaStream_t stream, float* zero_acc = nullptr);
 
 struct BwdMaps {
-  CUtensorMap q, k, v, dO;  // bf16, box 64 x 128 x 1, 128-byte swizzle
+  CUtensorMap q, k, v, dO;  // bf16, box 64 x 128 x 1 (k, v: 64 x 64 x 1 at d = 256), 128-byte swizzle
   CUtensorMap dq_acc;       // fp32 accumulator, box 32 x 128 x 1, 128-byte swizzle
   CUtensorMap dq_acc32;     // the same accumulator, box 32 x 32 x 1 (one warp's rows)
 };
@@ -153,6 +181,13 @@ cudaError_t launch_backward_d64(const BwdMaps& m, const float* lse, const float*
 cudaError_t launch_backward(const BwdMaps& m, const float* lse, const float* D, float* dq_acc,
                             void* dk, void* dv, const AttnShape& s, uint32_t* err,
                             cudaStream_t stream, bool with_dq = true);
+
+// dK and dV at head dimension 256 (fa_bwd_d256.cu): 64-key tiles, the
+// accumulators held transposed; K/V maps with 64-row boxes.  dQ follows from
+// launch_backward_dq.
+cudaError_t launch_backward_d256_kv(const BwdMaps& m, const float* lse, const float* D, void* dk,
+                                    void* dv, const AttnShape& s, uint32_t* err,
+                                    cudaStream_t stream);
 
 // dQ of the deterministic backward (fa_bwd_dq.cu): per query tile, key tiles
 // in forward order, dq = bf16(scale * dS K) written directly, no atomics.

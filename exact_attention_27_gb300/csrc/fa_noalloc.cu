@@ -16,7 +16,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -34,8 +33,6 @@ static __device__ __align__(256) unsigned char fa_noalloc_scratch[FA_NOALLOC_SCR
 // never for the device memory itself, so kernels must be given this address.
 void* scratch_address() { return fa::symbol_address_cached(fa_noalloc_scratch); }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" fa_status fa_backward_noalloc(const void* q, const void* k, const void* v,
@@ -43,41 +40,23 @@ extern "C" fa_status fa_backward_noalloc(const void* q, const void* k, const voi
                                          void* dq, void* dk, void* dv, int B, int H_q, int H_kv,
                                          int N, int d, float scale, int causal,
                                          cudaStream_t stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARGUMENT;
   // The checks of fa_backward, in the same order, so both return the same codes.
-  const fa_status st = fa::validate(B, H_q, H_kv, N, d, scale, causal);
+  const fa_status st = fa::validate_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H_q, H_kv, N, d,
+                                             scale, causal);
   if (st != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
-  const void* p16[] = {q, k, v, o, dO, dq, dk, dv};
-  for (const void* p : p16)
-    if (!aligned16(p)) return FA_ERR_INVALID_ARGUMENT;
-  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_INVALID_ARGUMENT;
-
-  // The scratch must hold D and the accumulator for every query row.
-  const double rows_d = static_cast<double>(B) * H_q * N;
-  const double need = std::ceil(rows_d * 4.0 / 1024.0) * 1024.0 + rows_d * d * 4.0;
-  if (need > static_cast<double>(FA_NOALLOC_SCRATCH_BYTES)) return FA_ERR_INVALID_ARGUMENT;
-  const long long rows = static_cast<long long>(B) * H_q * N;
-  const size_t acc_off = (static_cast<size_t>(rows) * 4 + 1023) & ~static_cast<size_t>(1023);
-
+  // The scratch must hold what fa_backward would take from the pool: D for
+  // every query row and, unless d = 256 (two kernels, no accumulator), the
+  // fp32 dQ accumulator.  validate() bounds B*H_q*N*d below 2^40, so the
+  // sizes cannot overflow.
+  size_t acc_off = 0;
+  const size_t need = fa::backward_scratch_bytes(B, H_q, N, d, false, &acc_off);
+  if (need > static_cast<size_t>(FA_NOALLOC_SCRATCH_BYTES)) return FA_ERR_INVALID_ARGUMENT;
   void* base = scratch_address();
-  uint32_t* err = fa::device_error_word();
-  if (!base || !err) return FA_ERR_CUDA;
+  if (!base) return FA_ERR_CUDA;
   float* Dbuf = static_cast<float*>(base);
-  float* acc = reinterpret_cast<float*>(static_cast<char*>(base) + acc_off);
-
-  fa::BwdMaps m;
-  const bool ok = fa::encode_map_bf16(&m.q, q, d, N, static_cast<long long>(B) * H_q) &&
-                  fa::encode_map_bf16(&m.k, k, d, N, static_cast<long long>(B) * H_kv) &&
-                  fa::encode_map_bf16(&m.v, v, d, N, static_cast<long long>(B) * H_kv) &&
-                  fa::encode_map_bf16(&m.dO, dO, d, N, static_cast<long long>(B) * H_q) &&
-                  fa::encode_map_f32_acc(&m.dq_acc, acc, d, N, static_cast<long long>(B) * H_q) &&
-                  fa::encode_map_f32_acc32(&m.dq_acc32, acc, d, N, static_cast<long long>(B) * H_q);
-  if (!ok) return FA_ERR_CUDA;
+  float* acc = acc_off ? reinterpret_cast<float*>(static_cast<char*>(base) + acc_off) : nullptr;
   fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
-  // The accumulator keeps the previous call's sums: the preprocess clears it.
-  cudaError_t e = fa::launch_preprocess(o, dO, Dbuf, rows, d, stream, acc);
-  if (e == cudaSuccess) e = fa::launch_backward(m, lse, Dbuf, acc, dk, dv, s, err, stream);
-  if (e == cudaSuccess) e = fa::launch_dq_finalize(acc, dq, rows * d, scale, stream);
-  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  // The accumulator keeps the previous call's sums: the row-dot pass clears it.
+  return fa::enqueue_backward(q, k, v, o, lse, dO, dq, dk, dv, s, Dbuf, acc,
+                              /*deterministic=*/false, /*timed=*/false, stream);
 }

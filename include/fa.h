@@ -34,7 +34,7 @@
  *     fa_last_device_error reports a timed-out wait inside a kernel.
  *   - Nothing is printed and nothing aborts.
  *
- * Supported sizes: d in {64, 96, 128} (and 256 for fa_forward and fa_forward_ex);
+ * Supported sizes: d in {64, 96, 128, 256} (fa_forward_fp8: 128 only);
  * B, H_q, H_kv, N >= 1; H_q % H_kv == 0;
  * B * H_q * N * d < 2^40.
  */
@@ -168,6 +168,12 @@ int fa_forward_tile_rows_for(int B, int H_q, int H_kv, int N_q, int N_kv, int d,
  * released the same way before the call returns; the caller's buffers are
  * not used as scratch.  dq/dk/dv must not alias any input.
  *
+ * At d = 256 the call runs the two kernels of fa_backward_deterministic (its
+ * results are then bit-reproducible) and takes only D as scratch: the fp32
+ * dK and dV of a 128-key tile would fill the whole tensor memory, so dK and
+ * dV come from 64-key tiles with the accumulators held transposed, and dQ
+ * from a kernel that owns query tiles.
+ *
  * Returns as fa_forward; FA_ERR_CUDA also when the scratch allocation fails.
  */
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o,
@@ -213,7 +219,8 @@ fa_status fa_backward_deterministic(const void* q, const void* k, const void* v,
  * inside the library, reserved on every GPU that loads the library until the
  * process exits.  It holds D and the fp32 dQ accumulator, so a call needs
  *     ceil(B*H_q*N*4 / 1024)*1024 + B*H_q*N*d*4  bytes
- * (for example B=2, H_q=8, N=4096, d=64: about 16.3 MiB); larger problems are
+ * (for example B=2, H_q=8, N=4096, d=64: about 16.3 MiB), or B*H_q*N*4 bytes
+ * at d = 256, where the backward has no accumulator; larger problems are
  * rejected with FA_ERR_INVALID_ARGUMENT before anything is launched.
  *
  * The array is shared by all calls on a device and keeps the last call's
@@ -238,7 +245,7 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
  *
  *   o, dO  [rows][d] bf16 device pointers, 16-byte aligned, read
  *   D      [rows]    fp32 device pointer, written
- * d in {64, 96, 128}; rows >= 1.  Same return codes as fa_forward.
+ * d in {64, 96, 128, 256}; rows >= 1.  Same return codes as fa_forward.
  */
 fa_status fa_backward_preprocess(const void* o, const void* dO, float* D, long long rows, int d,
                                  cudaStream_t stream);

@@ -82,12 +82,13 @@ def test_backward_rejects_invalid_arguments(lib, kw):
     assert bwd(lib, **kw) == fa.FA_ERR_INVALID_ARGUMENT
 
 
-@pytest.mark.parametrize("d", [80, 256])
+@pytest.mark.parametrize("d", [0, 32, 80, 160, 192, 512])
 def test_backward_rejects_unsupported_head_dim(lib, d):
-    """d = 256 has a forward kernel only."""
     assert bwd(lib, d=d) == fa.FA_ERR_UNSUPPORTED
     assert lib.fa_backward_deterministic(P, P, P, P, P, P, P, P, P, 1, 2, 1, 64, d,
                                          ctypes.c_float(0.125), 1, None) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_backward_noalloc(P, P, P, P, P, P, P, P, P, 1, 2, 1, 64, d,
+                                   ctypes.c_float(0.125), 1, None) == fa.FA_ERR_UNSUPPORTED
 
 
 def test_preprocess_rejects_invalid_arguments(lib):
@@ -95,6 +96,7 @@ def test_preprocess_rejects_invalid_arguments(lib):
     assert lib.fa_backward_preprocess(None, P, P, 4, 64, None) == fa.FA_ERR_INVALID_ARGUMENT
     assert lib.fa_backward_preprocess(Q, P, P, 4, 64, None) == fa.FA_ERR_INVALID_ARGUMENT
     assert lib.fa_backward_preprocess(P, P, P, 4, 48, None) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_backward_preprocess(P, P, P, 4, 512, None) == fa.FA_ERR_UNSUPPORTED
 
 
 def test_selftest_rejects_out_of_range_limit(lib):

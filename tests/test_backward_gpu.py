@@ -33,11 +33,12 @@ def run_fwd_bwd(inp, causal, scale):
     return o, lse, (dq, dk, dv)
 
 
-def bwd_vs_oracle(inp, causal, scale):
+def bwd_vs_oracle(inp, causal, scale, check_fwd=True):
     o, lse, grads = run_fwd_bwd(inp, causal, scale)
     f = {n: as_f64(inp[n]) for n in ("q", "k", "v", "do")}
-    o_ref, l_ref = oracle.attention_forward(f["q"], f["k"], f["v"], scale, causal)
-    check_forward(o, lse, o_ref, l_ref, "forward")
+    if check_fwd:
+        o_ref, l_ref = oracle.attention_forward(f["q"], f["k"], f["v"], scale, causal)
+        check_forward(o, lse, o_ref, l_ref, "forward")
     ref = oracle.attention_backward(f["q"], f["k"], f["v"], f["do"], scale, causal)
     check_grads(grads, ref, "backward")
     return grads
@@ -82,12 +83,54 @@ def test_head_dim_96(N, causal):
     bwd_vs_oracle(inp, causal, 1.0 / math.sqrt(96))
 
 
+@pytest.mark.parametrize("N", [1, 5, 63, 64, 65, 129, 200, 600])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_256(N, causal):
+    """d = 256: dK and dV from 64-key tiles with the accumulators held
+    transposed, then dQ from the query-tile kernel; GQA so that dK/dV sum over
+    two heads.  Ragged lengths around the 64-key and 128-query tiles."""
+    inp = make_inputs(1, 4, 2, N, 256, seed=N + 2560, with_grad=True)
+    bwd_vs_oracle(inp, causal, 1.0 / math.sqrt(256))
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_head_dim_256_grouped_query_heads(G):
+    inp = make_inputs(2, 8, 8 // G, 300, 256, seed=2570 + G, with_grad=True)
+    bwd_vs_oracle(inp, True, 1.0 / math.sqrt(256))
+
+
+def test_head_dim_256_large_scores():
+    """Scores spanning many log2 units (Q scaled by 3): P rebuilt from L must
+    stay exact.  Gradients only: with the softmax this sharp the forward's
+    absolute O error sits at the edge of the N(0,1)-input bound (bf16 P and O
+    times |v| up to ~5), which the forward tests cover on their own inputs."""
+    inp = make_inputs(1, 2, 1, 700, 256, seed=2580, with_grad=True)
+    inp["q"] = (inp["q"].float() * 3.0).to(torch.bfloat16)
+    bwd_vs_oracle(inp, True, 0.25, check_fwd=False)
+
+
+def test_head_dim_256_both_entry_points_agree_bit_for_bit():
+    """At d = 256 fa_backward runs the same two atomic-free kernels as
+    fa_backward_deterministic: identical bits, and run to run."""
+    import exact_attention_27_gb300 as fa
+    inp = make_inputs(1, 8, 2, 777, 256, seed=2590, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = nan_forward(q, k, v, causal=True)
+    g1 = nan_backward(q, k, v, o, lse, do, causal=True)
+    g2 = nan_backward(q, k, v, o, lse, do, causal=True, deterministic=True)
+    g3 = nan_backward(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == 0
+    for a, b, c in zip(g1, g2, g3):
+        assert torch.equal(a, b) and torch.equal(a, c)
+
+
 def test_d128_causal_mid_size():
     inp = make_inputs(1, 4, 4, 1024, 128, seed=123, with_grad=True)
     bwd_vs_oracle(inp, True, 1.0 / math.sqrt(128))
 
 
-@pytest.mark.parametrize("d", [64, 96, 128])
+@pytest.mark.parametrize("d", [64, 96, 128, 256])
 def test_preprocess_row_dot(d):
     """B1 alone: D = rowsum(dO o O) against the oracle's row_dot."""
     import exact_attention_27_gb300 as fa
@@ -141,6 +184,8 @@ def run_deterministic(inp, causal, scale):
     (1, 2, 2, 1, 64, True),
     (1, 4, 2, 333, 96, True),
     (1, 2, 1, 200, 96, False),
+    (1, 4, 2, 333, 256, True),
+    (1, 2, 1, 200, 256, False),
 ])
 def test_deterministic_backward_against_the_oracle(shape):
     B, Hq, Hkv, N, d, causal = shape
@@ -175,6 +220,8 @@ def test_deterministic_backward_is_bitwise_reproducible(d, G):
     (2, 16, 16, 4096, 128, True),    # the deterministic path at the same size
     (1, 2, 2, 32768, 64, False),     # long sequence: 256 query tiles for the first key tile
     (1, 2, 2, 32768, 64, True),      # and the deterministic path there
+    (2, 16, 16, 4096, 256, False),   # the d = 256 backward timed beside the step
+    (1, 8, 2, 8192, 256, True),      # d = 256, grouped-query heads, longer sequence
 ])
 def test_full_size_backward_sampled(B, Hq, Hkv, N, d, det):
     """Full-size causal backward against the oracle on two 256-row query
@@ -213,7 +260,7 @@ def test_full_size_backward_sampled(B, Hq, Hkv, N, d, det):
             assert err <= GRAD_REL * np.abs(r).max(), f"rows {r0}..: err {err:.3e}"
 
 
-@pytest.mark.parametrize("d", [64, 96, 128])
+@pytest.mark.parametrize("d", [64, 96, 128, 256])
 @pytest.mark.parametrize("det", [False, True])
 def test_many_heads_tiny_sequence(d, det):
     """B x H_q = 4096 heads of 17 positions, GQA 2: every CTA holds one

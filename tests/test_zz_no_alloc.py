@@ -79,6 +79,7 @@ class _Problem:
     ("causal_train_n4096_d64", None),
     ("non-causal GQA ragged d128", (1, 4, 2, 777, 128, False)),
     ("causal GQA d96", (1, 8, 2, 1000, 96, True)),
+    ("causal GQA d256", (1, 8, 2, 1000, 256, True)),
 ])
 def test_matches_the_oracle_and_fa_backward_on_two_calls_in_a_row(lib, shape):
     name, custom = shape
