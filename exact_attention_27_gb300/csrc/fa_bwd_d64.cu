@@ -75,8 +75,7 @@ struct Cfg64 {
   static constexpr int B_QDEMPTY = B_QDFULL + NSQ;
   static constexpr int B_SDP = B_QDEMPTY + NSQ;   // [2] S^T/dP^T of a half ready
   static constexpr int B_PDS = B_SDP + 2;         // [2] P^T/dS^T of a half ready (8 warp arrivals)
-  static constexpr int B_DSFREE = B_PDS + 2;      // [2] dS^T smem buffer of a tile free
-  static constexpr int B_DQFULL = B_DSFREE + 2;   // dQ of a tile in TMEM
+  static constexpr int B_DQFULL = B_PDS + 2;      // dQ of a tile in TMEM
   static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ drained (4 warp arrivals)
   static constexpr int B_WG = B_DQFREE + 1;       // drain-warpgroup internal sync (4 warp arrivals)
   static constexpr int B_LDFULL = B_WG + 1;       // [NLD] L/D slot filled (4 warp arrivals)
@@ -189,7 +188,6 @@ __global__ void __launch_bounds__(448, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::B_SDP + s), 1);
       mbar_init(bar(C::B_PDS + s), 8);  // both compute warpgroups
-      mbar_init(bar(C::B_DSFREE + s), 1);
     }
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQFREE), 4);
@@ -322,7 +320,6 @@ __global__ void __launch_bounds__(448, 1)
           for (int kk = 1; kk < 8; ++kk)
             mma_ss_k<ID_Q, 1>(tmem + C::COL_DQ, desc_add(dsd, kk * 2048), desc_add(k_mn, kk * 2048));
           mma_commit(bar(C::B_DQFULL));
-          mma_commit(bar(C::B_DSFREE + (s & 1)));
         }
         // Once, after the last half: everything issued has completed.  (A
         // barrier that completes once per tile could not tell its last phase
@@ -348,14 +345,13 @@ __global__ void __launch_bounds__(448, 1)
       int bhq, it;
       step_coords(s, bhq, it);
       const int q0 = it * C::BQ + a * 64 + wg * 32;  // first query of this warpgroup's columns
+      // S^T/dP^T of this half.  Its completion also means that the dQ product
+      // of tile s - 2 has read the dS^T buffer this tile writes again: that
+      // product was issued, by the same thread, before this half's S^T/dP^T,
+      // and a commit tracks every earlier tcgen05 operation of its thread.
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SDP + a), (h >> 1) & 1, abort_flag, p.err,
                                              kErrTimeoutSoftmax));
       if (!ok) break;
-      if (DQ && s >= 2 && a == 0) {  // the dS^T buffer of tile s - 2 must have been read by its dQ MMA
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DSFREE + (s & 1)), ((s - 2) >> 1) & 1,
-                                               abort_flag, p.err, kErrTimeoutSoftmax));
-        if (!ok) break;
-      }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_LDFULL + h % C::NLD), (h / C::NLD) & 1,
                                              abort_flag, p.err, kErrTimeoutSoftmax));
       if (!ok) break;
