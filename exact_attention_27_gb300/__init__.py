@@ -150,7 +150,7 @@ def fa_forward_fp8(q, k, v_t, o, lse, scale, causal, q_descale=1.0, k_descale=1.
 
 
 def fa_set_forward_tile_rows(rows):
-    """fa_set_forward_tile_rows of include/fa.h: 0 (per shape), 128 or 256."""
+    """fa_set_forward_tile_rows of include/fa.h: 0 (per shape), 128, 256 or 512."""
     _check(library().fa_set_forward_tile_rows(int(rows)), "fa_set_forward_tile_rows")
 
 

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_tile1.cu", "fa_bwd.cu", "fa_bwd_d64.cu",
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_tile1.cu", "fa_fwd_pair.cu", "fa_bwd.cu", "fa_bwd_d64.cu",
            "fa_bwd_d256.cu", "fa_bwd_dq.cu", "fa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,

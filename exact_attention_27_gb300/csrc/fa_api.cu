@@ -73,6 +73,24 @@ bool make_kv_map_bf16(CUtensorMap* m, const void* ptr, int d, int N, long long p
                   d == 256 ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Encodes the maps and launches the bf16 forward (one CTA per query tile or
+// pair of tiles, or a pair of CTAs at d = 128, whose K map has 64-row boxes).
+cudaError_t forward_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                         const fa::AttnShape& s, uint32_t* err, cudaStream_t stream) {
+  const long long qplanes = static_cast<long long>(s.B) * s.Hq;
+  const long long kvplanes = static_cast<long long>(s.B) * s.Hkv;
+  const bool pair = fa::forward_uses_pair(s);
+  CUtensorMap tq, tk, tv;
+  const bool ok = make_map_bf16(&tq, q, s.d, s.N, qplanes) &&
+                  (pair ? make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, s.d, s.keys(),
+                                   kvplanes, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
+                        : make_kv_map_bf16(&tk, k, s.d, s.keys(), kvplanes)) &&
+                  make_kv_map_bf16(&tv, v, s.d, s.keys(), kvplanes);
+  if (!ok) return cudaErrorInvalidValue;
+  return pair ? fa::launch_forward_pair(tq, tk, tv, o, lse, s, err, stream)
+              : fa::launch_forward(tq, tk, tv, o, lse, s, err, stream);
+}
+
 // A single thread waits on an mbarrier that nothing will ever complete, with
 // the caller's time limit, then records the timeout like the real kernels do.
 __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, uint32_t* err) {
@@ -195,16 +213,10 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return FA_ERR_INVALID_ARGUMENT;
-  CUtensorMap tq, tk, tv;
-  if (!make_map_bf16(&tq, q, d, N, static_cast<long long>(B) * H_q) ||
-      !make_kv_map_bf16(&tk, k, d, N, static_cast<long long>(B) * H_kv) ||
-      !make_kv_map_bf16(&tv, v, d, N, static_cast<long long>(B) * H_kv))
-    return FA_ERR_CUDA;
   uint32_t* err = error_word();
   if (!err) return FA_ERR_CUDA;
   fa::AttnShape s{B, H_q, H_kv, N, d, scale, causal};
-  return fa::launch_forward(tq, tk, tv, o, lse, s, err, stream) == cudaSuccess ? FA_OK
-                                                                               : FA_ERR_CUDA;
+  return forward_bf16(q, k, v, o, lse, s, err, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -219,18 +231,12 @@ fa_status fa_forward_ex(const void* q, const void* k, const void* v, void* o, fl
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return FA_ERR_INVALID_ARGUMENT;
-  CUtensorMap tq, tk, tv;
-  if (!make_map_bf16(&tq, q, d, N_q, static_cast<long long>(B) * H_q) ||
-      !make_kv_map_bf16(&tk, k, d, N_kv, static_cast<long long>(B) * H_kv) ||
-      !make_kv_map_bf16(&tv, v, d, N_kv, static_cast<long long>(B) * H_kv))
-    return FA_ERR_CUDA;
   uint32_t* err = error_word();
   if (!err) return FA_ERR_CUDA;
   fa::AttnShape s{B, H_q, H_kv, N_q, d, scale, causal};
   s.Nk = N_kv;
   s.q_offset = q_offset;
-  return fa::launch_forward(tq, tk, tv, o, lse, s, err, stream) == cudaSuccess ? FA_OK
-                                                                               : FA_ERR_CUDA;
+  return forward_bf16(q, k, v, o, lse, s, err, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o, float* lse,
@@ -340,7 +346,7 @@ fa_status fa_last_device_error(cudaStream_t stream) {
 }
 
 fa_status fa_set_forward_tile_rows(int rows) {
-  if (rows != 0 && rows != 128 && rows != 256) return FA_ERR_INVALID_ARGUMENT;
+  if (rows != 0 && rows != 128 && rows != 256 && rows != 512) return FA_ERR_INVALID_ARGUMENT;
   fa::set_forward_rows_per_cta(rows);
   return FA_OK;
 }

@@ -733,7 +733,7 @@ namespace {
 bool use_one_tile_per_cta(const AttnShape& s) {
   const int forced = g_rows_per_cta.load(std::memory_order_relaxed);
   if (forced == 128) return true;
-  if (forced == 256) return false;
+  if (forced == 256 || forced == 512) return false;
   static int sms = [] {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -745,6 +745,10 @@ bool use_one_tile_per_cta(const AttnShape& s) {
 }
 
 }  // namespace
+
+bool forward_uses_pair(const AttnShape& s) {
+  return s.d == 128 && g_rows_per_cta.load(std::memory_order_relaxed) == 512;
+}
 
 void set_forward_rows_per_cta(int rows) { g_rows_per_cta.store(rows); }
 int forward_rows_per_cta() { return g_rows_per_cta.load(); }

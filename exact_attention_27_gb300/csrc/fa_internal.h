@@ -152,7 +152,17 @@ void* symbol_address_cached(const T& symbol) {
   return cache[dev];
 }
 
-// Query rows per CTA for the forward: 0 = chosen per shape, 128 or 256.
+// The forward at d = 128 on a pair of CTAs (fa_fwd_pair.cu): four query
+// tiles per pair, products issued once for both CTAs.  tk must have 64 x 64
+// boxes (half a key tile), tq and tv the usual 64 x 128 boxes.
+cudaError_t launch_forward_pair(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, void* o, float* lse, const AttnShape& s,
+                                uint32_t* err, cudaStream_t stream);
+// Whether fa_forward / fa_forward_ex run shape s on a pair of CTAs.
+bool forward_uses_pair(const AttnShape& s);
+
+// Query rows per K/V-sharing unit of the forward: 0 = chosen per shape, 128,
+// 256, or 512 (a pair of CTAs; d = 128).
 void set_forward_rows_per_cta(int rows);
 // Query rows per CTA (128 or 256) that the bf16 forward chooses for shape s
 // on a GPU with `sms` multiprocessors when no setting forces one; host only.

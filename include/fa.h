@@ -127,9 +127,14 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o,
  * optimización", does per sequence length:
  *   0    chosen per shape (the default), as fa_forward_tile_rows_for says;
  *   128  one 128-row query tile per CTA;
- *   256  two 128-row query tiles per CTA sharing each K/V tile.
- * Both give the same results up to rounding order.  d = 256 always uses
- * 128.  Process-wide; returns FA_ERR_INVALID_ARGUMENT for any other value.
+ *   256  two 128-row query tiles per CTA sharing each K/V tile;
+ *   512  at d = 128: a pair of CTAs (a cluster of two) with two query tiles
+ *        each, whose tensor-core products are issued once for both CTAs
+ *        (M = 256 across the pair) and which each load half of every K/V
+ *        tile; at other d as 256.
+ * All give the same results up to rounding order (256 and 512 the same
+ * bits).  d = 256 always uses 128.  Process-wide; returns
+ * FA_ERR_INVALID_ARGUMENT for any other value.
  */
 fa_status fa_set_forward_tile_rows(int rows);
 

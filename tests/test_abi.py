@@ -154,7 +154,7 @@ def test_forward_fp8_rejects_unsupported_head_dim(lib, d):
     assert fwd_fp8(lib, d=d) == fa.FA_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("rows", [-1, 1, 64, 127, 512])
+@pytest.mark.parametrize("rows", [-1, 1, 64, 127, 384, 1024])
 def test_forward_tile_rows_rejects_other_values(lib, rows):
     assert lib.fa_set_forward_tile_rows(rows) == fa.FA_ERR_INVALID_ARGUMENT
     assert lib.fa_set_forward_tile_rows(0) == fa.FA_OK

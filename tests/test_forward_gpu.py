@@ -314,3 +314,42 @@ def test_long_sequence_one_head(tile_rows, rows_per_cta, d):
     rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, N - 129, N - 128, N - 1],
                                      rng.integers(0, N, 16)]))
     forward_vs_oracle(inp, True, 1.0 / math.sqrt(d), rows=rows)
+
+
+@pytest.mark.parametrize("N,causal,Hq,Hkv", [
+    (1, True, 2, 1), (129, False, 2, 2), (300, True, 4, 2), (513, True, 2, 2),
+    (1000, False, 2, 1), (1024, True, 4, 4), (2048, True, 8, 2), (777, True, 2, 2),
+])
+def test_cta_pair_forward_against_the_oracle(tile_rows, N, causal, Hq, Hkv):
+    """d = 128 on a pair of CTAs (M = 256 products across the two, four query
+    tiles per pair): ragged tails, quads with tiles past N, GQA."""
+    tile_rows(512)
+    inp = make_inputs(1, Hq, Hkv, N, 128, seed=N + 512)
+    forward_vs_oracle(inp, causal, 1.0 / math.sqrt(128))
+
+
+@pytest.mark.parametrize("N,causal", [(1000, True), (2048, False), (4096, True)])
+def test_cta_pair_forward_equals_the_two_tile_forward(tile_rows, N, causal):
+    """Both kernels form every score and every P V sum in the same order, so
+    the pair's outputs equal the two-tile CTA's bit for bit."""
+    inp = make_inputs(2, 4, 2, N, 128, seed=N + 5120)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    tile_rows(256)
+    o1, l1 = nan_forward(q, k, v, causal=causal)
+    tile_rows(512)
+    o2, l2 = nan_forward(q, k, v, causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_cta_pair_forward_with_query_offset(tile_rows):
+    import exact_attention_27_gb300 as fa
+    tile_rows(512)
+    inp = make_inputs(1, 4, 2, 300, 128, seed=5130, Nk=941)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    o, lse = nan_forward(q, k, v, causal=True, scale=0.1, q_offset=641)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_error() == 0
+    o_ref, l_ref = oracle.attention_forward(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]),
+                                            0.1, True, q_offset=641)
+    check_forward(o, lse, o_ref, l_ref, "pair offset")
