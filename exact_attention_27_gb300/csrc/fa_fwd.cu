@@ -546,11 +546,15 @@ __global__ void __launch_bounds__(384, 1)
       sum += sum_hi;
       l = l * alpha + sum;
       // O holds P_0..P_{j-1} contributions; it must be final before it is
-      // rescaled.  With ROT3 nothing else waits for it, so the wait is made
-      // only when a rescale is due (O += P_x(j) V waits for this tile's P, so
-      // the barrier cannot run two phases ahead).
+      // rescaled.  The S just waited for was issued, by the same thread,
+      // after O += P_x(j-1) V (with ROT3 after the P V that read its buffer
+      // before), and a commit tracks every earlier tcgen05 operation of its
+      // thread, so that product has completed and P_x(j) may overwrite the
+      // columns it read; the wait below is kept for the rescale alone and
+      // returns at once.  (O += P_x(j) V waits for this tile's P, so the
+      // barrier is never two phases ahead of a waiter.)
       const bool resc = j > 0 && __any_sync(0xffffffffu, upd);
-      if (j > 0 && (resc || !C::ROT3)) {
+      if (resc) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
                                                p.err, kErrTimeoutSoftmax));
         if (!ok) break;

@@ -400,10 +400,13 @@ __global__ void __launch_bounds__(384, 1)
       sum += sum_hi;
       l = l * alpha + sum;
       // O holds P_0..P_{j-1} contributions; it must be final before it is
-      // rescaled.  O += P_x(j) V waits for this tile's P (in both CTAs), so
-      // the barrier cannot run two phases ahead.
+      // rescaled.  S_x(j) was issued after O += P_x(j-1) V by the same
+      // thread, whose commit tracks every earlier product, so that product
+      // has completed once S_x(j) has; the wait is kept for the rescale alone.
+      // O += P_x(j) V waits for this tile's P (in both CTAs), so the barrier
+      // is never two phases ahead of a waiter.
       const bool resc = j > 0 && __any_sync(0xffffffffu, upd);
-      if (j > 0) {
+      if (resc) {
         ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(C::B_ODONE + x), (j - 1) & 1,
                                                        abort_flag, p.err, kErrTimeoutSoftmax));
         if (!ok) break;
