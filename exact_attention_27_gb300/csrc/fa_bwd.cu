@@ -145,9 +145,11 @@ struct BwdCfg {
   static constexpr int B_QEMPTY = B_QFULL + NQ;   // [NQ]
   static constexpr int B_DOFULL = B_QEMPTY + NQ;
   static constexpr int B_DOEMPTY = B_DOFULL + 1;
-  static constexpr int B_SDP = B_DOEMPTY + 1;     // S^T and dP^T in TMEM
-  static constexpr int B_PDS = B_SDP + 1;         // P^T in TMEM and dS^T in smem (128 arrivals)
-  static constexpr int B_DQFULL = B_PDS + 1;      // dQ in TMEM, all MMAs of the step done
+  static constexpr int B_S = B_DOEMPTY + 1;       // S^T in TMEM
+  static constexpr int B_DP = B_S + 1;            // dP^T in TMEM
+  static constexpr int B_P = B_DP + 1;            // P^T in TMEM, S^T read (128 arrivals)
+  static constexpr int B_DS = B_P + 1;            // dS^T in smem, dP^T read (128 arrivals)
+  static constexpr int B_DQFULL = B_DS + 1;       // dQ in TMEM, all MMAs of the step done
   static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ columns drained (128 arrivals)
   static constexpr int B_WG = B_DQFREE + 1;      // key-row warpgroup sync (128 arrivals)
   static constexpr int B_DRAIN = B_WG + 1;
@@ -260,8 +262,10 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(bar(C::B_DOFULL), 1);
     mbar_init(bar(C::B_DOEMPTY), 1);
-    mbar_init(bar(C::B_SDP), 1);
-    mbar_init(bar(C::B_PDS), 128);
+    mbar_init(bar(C::B_S), 1);
+    mbar_init(bar(C::B_DP), 1);
+    mbar_init(bar(C::B_P), 128);
+    mbar_init(bar(C::B_DS), 128);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQFREE), 128);
     mbar_init(bar(C::B_WG), 128);
@@ -342,33 +346,50 @@ __global__ void __launch_bounds__(384, 1)
         constexpr uint32_t id_kd = idesc_bf16_f32(128, D, false, true);  // dV, dK
         constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);    // dQ
         bool ok = mbar_wait(bar(C::B_KV), 0, abort_flag, p.err, kErrTimeoutMma);
-        for (int s = 0; ok && s < n_steps; ++s) {
+        // S^T of step s (Q_s in stage s % NQ) into the S^T columns.
+        auto issue_s = [&](int s) -> bool {
           const int qs = s % C::NQ;
-          const uint32_t q_st = sQ + qs * C::TILE;
-          const uint32_t do_st = sdO;
           if (!mbar_wait(bar(C::B_QFULL + qs), (s / C::NQ) & 1, abort_flag, p.err, kErrTimeoutMma))
-            break;
+            return false;
           tc_fence_after();
+          const uint32_t q_st = sQ + qs * C::TILE;
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
             mma_ss(tmem + C::COL_S, smem_desc_sw128(sK + off, 16, 1024),
                    smem_desc_sw128(q_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
           }
-          if (s > 0) {
-            // dQ of the previous step lives in dP^T's columns until drained.
-            if (!mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma)) break;
-          }
-          if (!mbar_wait(bar(C::B_DOFULL), s & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+          mma_commit(bar(C::B_S));
+          return true;
+        };
+        // dP^T of step s into the dP^T columns, which hold dQ of step s - 1
+        // until the drain has taken it.
+        auto issue_dp = [&](int s) -> bool {
+          if (s > 0 &&
+              !mbar_wait(bar(C::B_DQFREE), (s - 1) & 1, abort_flag, p.err, kErrTimeoutMma))
+            return false;
+          if (!mbar_wait(bar(C::B_DOFULL), s & 1, abort_flag, p.err, kErrTimeoutMma)) return false;
           tc_fence_after();
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::SUB_BYTES + (kk & 3) * 32;
             mma_ss(tmem + C::COL_DP, smem_desc_sw128(sV + off, 16, 1024),
-                   smem_desc_sw128(do_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
+                   smem_desc_sw128(sdO + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(C::B_SDP));
-          if (!mbar_wait(bar(C::B_PDS), s & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+          mma_commit(bar(C::B_DP));
+          return true;
+        };
+        if (ok && n_steps > 0) ok = issue_s(0) && issue_dp(0);
+        // Per step: dV once the threads have written P^T, then the next S^T
+        // over it (the tensor pipe runs in issue order); dK and dQ once they
+        // have written dS^T, then the next dP^T once the drain has taken dQ.
+        // The threads compute dS^T while dV and the next S^T run, and the
+        // next step's P^T while dK, dQ, the drain and the next dP^T run.
+        for (int s = 0; ok && s < n_steps; ++s) {
+          const int qs = s % C::NQ;
+          const uint32_t q_st = sQ + qs * C::TILE;
+          const uint32_t do_st = sdO;
+          if (!mbar_wait(bar(C::B_P), s & 1, abort_flag, p.err, kErrTimeoutMma)) break;
           tc_fence_after();
           // dV += P^T dO_i   (A = P^T in TMEM: 16 queries = 8 packed columns per step)
   #pragma unroll
@@ -377,6 +398,9 @@ __global__ void __launch_bounds__(384, 1)
                    smem_desc_sw128(do_st + kk * 2048, C::SUB_BYTES, 1024), id_kd,
                    (s > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(C::B_DOEMPTY));  // dO_i is not read after dV
+          if (s + 1 < n_steps && !issue_s(s + 1)) break;
+          if (!mbar_wait(bar(C::B_DS), s & 1, abort_flag, p.err, kErrTimeoutMma)) break;
+          tc_fence_after();
           // dK += dS^T Q_i   (A = dS^T K-major: queries contiguous per key row)
   #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -392,6 +416,7 @@ __global__ void __launch_bounds__(384, 1)
             mma_ss(tmem + C::COL_DQ, smem_desc_sw128(sDS + kk * 2048, C::SUB_BYTES, 1024),
                    smem_desc_sw128(sK + kk * 2048, C::SUB_BYTES, 1024), id_q, kk > 0 ? 1u : 0u);
           mma_commit(bar(C::B_DQFULL));
+          if (s + 1 < n_steps && !issue_dp(s + 1)) break;
         }
         if (*abort_flag) {
           mma_commit(bar(C::B_DRAIN));
@@ -432,9 +457,10 @@ __global__ void __launch_bounds__(384, 1)
     };
     float l_cur = 0.0f, d_cur = 0.0f;
     if (n_steps > 0) load_ld(0, l_cur, d_cur);
-    // Step s + 1's dS^T overwrites step s's in shared memory: its S^T/dP^T
-    // are computed only after the drain has read step s's dQ, by which time
-    // every product of step s (the ones reading dS^T too) has completed.
+    // Step s + 1's dS^T overwrites step s's in shared memory: it is written
+    // once dP^T of step s + 1 is in, which is computed only after the drain
+    // has taken step s's dQ, so every product of step s (the ones reading
+    // dS^T too) has completed.
     for (int s = 0; s < n_steps; ++s) {
       const int g = s / per_head;
       const int it = i0 + (s - g * per_head);
@@ -445,7 +471,7 @@ __global__ void __launch_bounds__(384, 1)
       if (s + 1 < n_steps) load_ld(s + 1, l_cur, d_cur);  // used at the next step
       if (!(ok = wg_sync())) break;
       ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar(C::B_SDP), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));
+                      mbar_wait(bar(C::B_S), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
       const float4* L4b = reinterpret_cast<const float4*>(sL + buf * 128);  // -L log2e
@@ -453,79 +479,105 @@ __global__ void __launch_bounds__(384, 1)
       // Masking is needed only on the diagonal tile and for keys past N.
       const bool masked = __any_sync(0xffffffffu, (CAUSAL && it == jt) || !key_live);
       const uint64_t c2 = f2_pack(c, c);
-      // Chunk cc + 1 (32 query columns of S^T and dP^T) is loaded while
-      // chunk cc is computed: tcgen05.wait::ld waits for every load issued,
-      // so each wait covers only loads that had a chunk's arithmetic to land.
-      // The P^T of chunk cc goes to columns 16cc.., below the S^T columns
-      // 32(cc + 1).. being loaded.
-      uint32_t sv2[2][32], dpv2[2][32];
-      tmem_ld32(tmem + lane_off + C::COL_S, sv2[0]);
-      tmem_ld32(tmem + lane_off + C::COL_DP, dpv2[0]);
-      tmem_wait_ld();
+      // ---- P^T = exp2(S^T c - L log2e), kept as packed bf16 for dS^T.
+      // Chunk cc + 1 (32 query columns) is loaded while chunk cc is
+      // computed; P^T of chunk cc goes to columns 16cc.., below the S^T
+      // columns 32(cc + 1).. being loaded.
+      uint32_t pk[64];
+      {
+        uint32_t sv2[2][32];
+        tmem_ld32(tmem + lane_off + C::COL_S, sv2[0]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        if (cc + 1 < 4) {
-          tmem_ld32(tmem + lane_off + C::COL_S + (cc + 1) * 32, sv2[(cc + 1) & 1]);
-          tmem_ld32(tmem + lane_off + C::COL_DP + (cc + 1) * 32, dpv2[(cc + 1) & 1]);
-        }
-        const uint32_t(&sv)[32] = sv2[cc & 1];
-        const uint32_t(&dpv)[32] = dpv2[cc & 1];
-        uint32_t pk[16], dk16[16];
+        for (int cc = 0; cc < 4; ++cc) {
+          if (cc + 1 < 4) tmem_ld32(tmem + lane_off + C::COL_S + (cc + 1) * 32, sv2[(cc + 1) & 1]);
+          const uint32_t(&sv)[32] = sv2[cc & 1];
 #pragma unroll
-        for (int u4 = 0; u4 < 8; ++u4) {
-          const float4 nl = L4b[cc * 8 + u4];
-          const float4 nd = D4b[cc * 8 + u4];
-          float pv[4];
-          // exp2 argument s c - L log2e on pairs
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[4 * u4]), __uint_as_float(sv[4 * u4 + 1])),
-                           c2, f2_pack(nl.x, nl.y)),
-                    pv[0], pv[1]);
-          f2_unpack(
-              f2_fma(f2_pack(__uint_as_float(sv[4 * u4 + 2]), __uint_as_float(sv[4 * u4 + 3])),
-                     c2, f2_pack(nl.z, nl.w)),
-              pv[2], pv[3]);
+          for (int u4 = 0; u4 < 8; ++u4) {
+            const float4 nl = L4b[cc * 8 + u4];
+            float pv[4];
+            f2_unpack(
+                f2_fma(f2_pack(__uint_as_float(sv[4 * u4]), __uint_as_float(sv[4 * u4 + 1])), c2,
+                       f2_pack(nl.x, nl.y)),
+                pv[0], pv[1]);
+            f2_unpack(
+                f2_fma(f2_pack(__uint_as_float(sv[4 * u4 + 2]), __uint_as_float(sv[4 * u4 + 3])),
+                       c2, f2_pack(nl.z, nl.w)),
+                pv[2], pv[3]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) pv[e] = ex2_approx(pv[e]);
-          if (masked) {
+            for (int e = 0; e < 4; ++e) pv[e] = ex2_approx(pv[e]);
+            if (masked) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (!key_live || (CAUSAL && key > q0 + cc * 32 + u4 * 4 + e)) pv[e] = 0.0f;
+              for (int e = 0; e < 4; ++e)
+                if (!key_live || (CAUSAL && key > q0 + cc * 32 + u4 * 4 + e)) pv[e] = 0.0f;
+            }
+            pk[cc * 16 + 2 * u4] = pack_bf16x2(pv[0], pv[1]);
+            pk[cc * 16 + 2 * u4 + 1] = pack_bf16x2(pv[2], pv[3]);
           }
-          // dS = P o (dP - D) on pairs
-          const uint64_t ds01 = f2_mul(
-              f2_pack(pv[0], pv[1]),
-              f2_add(f2_pack(__uint_as_float(dpv[4 * u4]), __uint_as_float(dpv[4 * u4 + 1])),
-                     f2_pack(nd.x, nd.y)));
-          const uint64_t ds23 = f2_mul(
-              f2_pack(pv[2], pv[3]),
-              f2_add(f2_pack(__uint_as_float(dpv[4 * u4 + 2]), __uint_as_float(dpv[4 * u4 + 3])),
-                     f2_pack(nd.z, nd.w)));
-          float dsv[4];
-          f2_unpack(ds01, dsv[0], dsv[1]);
-          f2_unpack(ds23, dsv[2], dsv[3]);
-          pk[2 * u4] = pack_bf16x2(pv[0], pv[1]);
-          pk[2 * u4 + 1] = pack_bf16x2(pv[2], pv[3]);
-          dk16[2 * u4] = pack_bf16x2(dsv[0], dsv[1]);
-          dk16[2 * u4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          tmem_st16(tmem + lane_off + C::COL_S + cc * 16,
+                    *reinterpret_cast<const uint32_t(*)[16]>(&pk[cc * 16]));
+          if (cc + 1 < 4) tmem_wait_ld();
         }
-        // P^T (bf16) over the S^T columns already read: queries cc*32.. -> columns cc*16..
-        tmem_st16(tmem + lane_off + C::COL_S + cc * 16, pk);
-        // dS^T row `t`, queries cc*32 .. cc*32+31: 4 chunks of 8 in block cc/2.
-        const uint32_t blk = sDS + (cc >> 1) * C::SUB_BYTES;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          st_shared_v4(blk + sw128(t, (cc & 1) * 4 + q4), dk16[4 * q4], dk16[4 * q4 + 1],
-                       dk16[4 * q4 + 2], dk16[4 * q4 + 3]);
-        if (cc + 1 < 4) tmem_wait_ld();
       }
       tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_P));
+      // ---- dS^T = P^T o (dP^T - D) from the bf16 P^T (as the dV product
+      // uses it), into the dS^T buffer in shared memory.
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::B_DP), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t dpv2[2][32];
+        tmem_ld32(tmem + lane_off + C::COL_DP, dpv2[0]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          if (cc + 1 < 4)
+            tmem_ld32(tmem + lane_off + C::COL_DP + (cc + 1) * 32, dpv2[(cc + 1) & 1]);
+          const uint32_t(&dpv)[32] = dpv2[cc & 1];
+          uint32_t dk16[16];
+#pragma unroll
+          for (int u4 = 0; u4 < 8; ++u4) {
+            const float4 nd = D4b[cc * 8 + u4];
+            const __nv_bfloat162 pa =
+                *reinterpret_cast<const __nv_bfloat162*>(&pk[cc * 16 + 2 * u4]);
+            const __nv_bfloat162 pb =
+                *reinterpret_cast<const __nv_bfloat162*>(&pk[cc * 16 + 2 * u4 + 1]);
+            const float2 p01 = __bfloat1622float2(pa);
+            const float2 p23 = __bfloat1622float2(pb);
+            const uint64_t ds01 = f2_mul(
+                f2_pack(p01.x, p01.y),
+                f2_add(f2_pack(__uint_as_float(dpv[4 * u4]), __uint_as_float(dpv[4 * u4 + 1])),
+                       f2_pack(nd.x, nd.y)));
+            const uint64_t ds23 = f2_mul(
+                f2_pack(p23.x, p23.y),
+                f2_add(
+                    f2_pack(__uint_as_float(dpv[4 * u4 + 2]), __uint_as_float(dpv[4 * u4 + 3])),
+                    f2_pack(nd.z, nd.w)));
+            float dsv[4];
+            f2_unpack(ds01, dsv[0], dsv[1]);
+            f2_unpack(ds23, dsv[2], dsv[3]);
+            dk16[2 * u4] = pack_bf16x2(dsv[0], dsv[1]);
+            dk16[2 * u4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          }
+          // dS^T row `t`, queries cc*32 .. cc*32+31: 4 chunks of 8 in block cc/2.
+          const uint32_t blk = sDS + (cc >> 1) * C::SUB_BYTES;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            st_shared_v4(blk + sw128(t, (cc & 1) * 4 + q4), dk16[4 * q4], dk16[4 * q4 + 1],
+                         dk16[4 * q4 + 2], dk16[4 * q4 + 3]);
+          if (cc + 1 < 4) tmem_wait_ld();
+        }
+      }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(C::B_PDS));
+      mbar_arrive(bar(C::B_DS));
     }
     // ---- epilogue: dK (times scale) and dV, one key row per thread, once the
     // last step's products have completed (the earlier steps' completed before
-    // the last step's S^T/dP^T were computed, so one phase is outstanding).
+    // the last step's dP^T was computed, so one phase is outstanding).
     if (ok && n_steps > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQFULL), (n_steps - 1) & 1, abort_flag,
                                              p.err, kErrTimeoutEpilogue));
