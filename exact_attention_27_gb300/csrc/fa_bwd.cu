@@ -149,10 +149,11 @@ struct BwdCfg {
   static constexpr int B_DP = B_S + 1;            // dP^T in TMEM
   static constexpr int B_P = B_DP + 1;            // P^T in TMEM, S^T read (128 arrivals)
   static constexpr int B_DS = B_P + 1;            // dS^T in smem, dP^T read (128 arrivals)
-  static constexpr int B_DQFULL = B_DS + 1;       // dQ in TMEM, all MMAs of the step done
+  static constexpr int B_DQFULL = B_DS + 1;       // dQ in TMEM (dV, dP^T, dQ of the step done)
   static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ columns drained (128 arrivals)
   static constexpr int B_WG = B_DQFREE + 1;      // key-row warpgroup sync (128 arrivals)
-  static constexpr int B_DRAIN = B_WG + 1;
+  static constexpr int B_FINAL = B_WG + 1;        // every product issued has completed (once)
+  static constexpr int B_DRAIN = B_FINAL + 1;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -269,6 +270,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQFREE), 128);
     mbar_init(bar(C::B_WG), 128);
+    mbar_init(bar(C::B_FINAL), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -401,6 +403,13 @@ __global__ void __launch_bounds__(384, 1)
           if (s + 1 < n_steps && !issue_s(s + 1)) break;
           if (!mbar_wait(bar(C::B_DS), s & 1, abort_flag, p.err, kErrTimeoutMma)) break;
           tc_fence_after();
+          // dQ_i = dS K_j first (A = dS: the dS^T buffer read MN-major; B = K_j
+          // MN-major), so that the drain takes it while dK runs.
+  #pragma unroll
+          for (int kk = 0; kk < (DQ ? 8 : 0); ++kk)
+            mma_ss(tmem + C::COL_DQ, smem_desc_sw128(sDS + kk * 2048, C::SUB_BYTES, 1024),
+                   smem_desc_sw128(sK + kk * 2048, C::SUB_BYTES, 1024), id_q, kk > 0 ? 1u : 0u);
+          mma_commit(bar(C::B_DQFULL));
           // dK += dS^T Q_i   (A = dS^T K-major: queries contiguous per key row)
   #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -410,12 +419,9 @@ __global__ void __launch_bounds__(384, 1)
                    (s > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar(C::B_QEMPTY + qs));  // Q_i is not read after dK
-          // dQ_i = dS K_j    (A = dS: the dS^T buffer read MN-major; B = K_j MN-major)
-  #pragma unroll
-          for (int kk = 0; kk < (DQ ? 8 : 0); ++kk)
-            mma_ss(tmem + C::COL_DQ, smem_desc_sw128(sDS + kk * 2048, C::SUB_BYTES, 1024),
-                   smem_desc_sw128(sK + kk * 2048, C::SUB_BYTES, 1024), id_q, kk > 0 ? 1u : 0u);
-          mma_commit(bar(C::B_DQFULL));
+          // Once, after the last step: every product has completed (the dK
+          // accumulator is final).
+          if (s == n_steps - 1) mma_commit(bar(C::B_FINAL));
           if (s + 1 < n_steps && !issue_dp(s + 1)) break;
         }
         if (*abort_flag) {
@@ -575,12 +581,11 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(bar(C::B_DS));
     }
-    // ---- epilogue: dK (times scale) and dV, one key row per thread, once the
-    // last step's products have completed (the earlier steps' completed before
-    // the last step's dP^T was computed, so one phase is outstanding).
+    // ---- epilogue: dK (times scale) and dV, one key row per thread, once
+    // every product has completed.
     if (ok && n_steps > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_DQFULL), (n_steps - 1) & 1, abort_flag,
-                                             p.err, kErrTimeoutEpilogue));
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(C::B_FINAL), 0, abort_flag, p.err, kErrTimeoutEpilogue));
     if (ok) {
       // dK (times scale); the drain warpgroup writes dV meanwhile.
       tc_fence_after();
