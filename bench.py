@@ -53,7 +53,7 @@ def peaks():
 # The source file of each kernel named in profiles/traffic.txt.
 KERNEL_SOURCES = {"fa_bwd64_kernel": "fa_bwd_d64.cu", "fa_fwd_kernel": "fa_fwd.cu",
                   "fa_fwd1_kernel": "fa_fwd_tile1.cu", "fa_bwd_kernel": "fa_bwd.cu",
-                  "fa_bwd_dq_kernel": "fa_bwd_dq.cu"}
+                  "fa_bwd_dq_kernel": "fa_bwd_dq.cu", "fa_bwd256_kv_kernel": "fa_bwd_d256.cu"}
 
 
 def kernel_traffic(kernel):
@@ -69,6 +69,21 @@ def kernel_traffic(kernel):
             if parts[3] == src_hash:
                 return float(parts[2])
     return None
+
+
+def workload_traffic(workload):
+    """{kernel: DRAM bytes per launch} for every kernel of a workload named in
+    the committed ncu summary whose source is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[1] == workload:
+            if parts[3] == source_hash(parts[0]):
+                out[parts[0]] = int(parts[2])
+    return out
 
 
 def source_hash(kernel):
@@ -563,7 +578,8 @@ def forward_workloads(fa, torch, tflops_peak, peak_src):
         tf = w.fwd_flops() / (ms * 1e-3) / 1e12
         line = {"workload": w.describe(), "ms": round(ms, 4), "tflops": round(tf, 1),
                 "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst",
-                "input_sets": R, "per_launch_ms": per_launch_ms(torch, launch)}
+                "input_sets": R, "per_launch_ms": per_launch_ms(torch, launch),
+                "dram_bytes_per_launch": workload_traffic(name) or None}
         if name == GRAPH_FWD_WORKLOAD:
             line["graph"] = graph_launches(torch, launch)
         out.append(line)
@@ -594,7 +610,8 @@ def backward_workloads(fa, torch, tflops_peak, peak_src):
     """fa_backward (or fa_backward_deterministic) alone, inputs resident,
     back-to-back calls; FLOPs 10 B H N^2 d / 2 (causal)."""
     out = []
-    for name, (B, Hq, Hkv, N, d), det in BWD_WORKLOADS:
+    short = {i: n for n, i in BWD_NAMES.items()}
+    for idx, (name, (B, Hq, Hkv, N, d), det) in enumerate(BWD_WORKLOADS):
         inp = make_inputs(B, Hq, Hkv, N, d, seed=11, with_grad=True)
         q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
         scale = 1.0 / math.sqrt(d)
@@ -616,7 +633,7 @@ def backward_workloads(fa, torch, tflops_peak, peak_src):
         pl = per_launch_ms(torch, lambda i: call(q, k, v, o, lse, do, dq, dk, dv, scale, True))
         out.append({"workload": name, "ms": round(ms, 4), "tflops": round(tf, 1),
                     "frac": round(tf / tflops_peak, 4), "peak": f"{peak_src} bf16 burst",
-                    "per_launch_ms": pl})
+                    "per_launch_ms": pl, "dram_bytes_per_launch": workload_traffic(short[idx]) or None})
         del q, k, v, do, o, lse, dq, dk, dv
         torch.cuda.empty_cache()
     return out
