@@ -133,7 +133,8 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v_t, void* o,
  *        (M = 256 across the pair) and which each load half of every K/V
  *        tile; at other d as 256.
  * All give the same results up to rounding order (256 and 512 the same
- * bits).  d = 256 always uses 128.  Process-wide; returns
+ * bits).  d = 256 always uses 128; fa_forward_fp8 always uses 256.
+ * Process-wide; returns
  * FA_ERR_INVALID_ARGUMENT for any other value.
  */
 fa_status fa_set_forward_tile_rows(int rows);

@@ -74,8 +74,9 @@ def bound(ex, scale, causal, o_ref, v_ds):
 def run_fp8(q8, k8, vt8, scale, causal, ds):
     import exact_attention_27_gb300 as fa
     q, k, vt = q8.cuda(), k8.cuda(), vt8.cuda()
-    o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
+    # NaN-filled, so that an element the kernel does not write fails the checks.
+    o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full(q.shape[:-1], float("nan"), dtype=torch.float32, device="cuda")
     fa.fa_forward_fp8(q, k, vt, o, lse, scale, causal, *ds)
     torch.cuda.synchronize()
     assert fa.fa_last_device_error() == 0
@@ -114,3 +115,20 @@ def test_fp8_causal_first_row_is_v0():
     o, _ = run_fp8(q8, k8, vt8, 1.0 / math.sqrt(d), True, ds)
     want = torch.from_numpy(ex["v"][:, :, 0]).to(torch.bfloat16).double().numpy()
     assert np.array_equal(o[:, :, 0], want)
+
+
+def test_fp8_forward_ignores_the_tile_rows_setting():
+    """The FP8 forward has one kernel (two 128-row query tiles per CTA);
+    fa_set_forward_tile_rows leaves its output unchanged, bit for bit."""
+    import exact_attention_27_gb300 as fa
+    d = 128
+    q8, k8, vt8, ex = fp8_inputs(1, 4, 2, 1000, d, seed=8123)
+    outs = []
+    try:
+        for rows in (0, 128, 256, 512):
+            fa.fa_set_forward_tile_rows(rows)
+            outs.append(run_fp8(q8, k8, vt8, 1.0 / math.sqrt(d), True, (1.0, 1.0, 1.0)))
+    finally:
+        fa.fa_set_forward_tile_rows(0)
+    for o, lse in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(lse, outs[0][1])
