@@ -116,9 +116,16 @@ struct FwdCfg {
   static constexpr bool ROT3 = (DP == 64) && !FP8;
   static constexpr int NSB = ROT3 ? 3 : 2;       // S buffers
   static constexpr int B_SFULL = B_VEMPTY + NS;  // [NSB] S in buffer (ROT3) or of tile x
-  static constexpr int B_PFULL = B_SFULL + NSB;  // [2] per query tile (4 warp arrivals)
-  static constexpr int B_ODONE = B_PFULL + 2;    // [2] per query tile
-  static constexpr int B_DRAIN = B_ODONE + 2;    // abort path: MMAs in flight
+  // P written over the S of buffer b (4 warp arrivals).  With ROT3 a tile's
+  // softmax may finish two steps before the MMA issuer waits for the first
+  // of them (say while it waits for a late V tile), so the barrier is per
+  // buffer: the buffer's next P needs an S issued after this P's P V, and
+  // the barrier is never two phases ahead of the issuer.  Without ROT3 a
+  // tile's next S follows its own P V, and buffer x is tile x's.
+  static constexpr int B_PFULL = B_SFULL + NSB;  // [NSB]
+  static constexpr int B_ODONE = B_PFULL + NSB;  // [2] per query tile: O += P V done
+  static constexpr int B_OFIN = B_ODONE + 2;     // [2] per query tile, once: its last P V done
+  static constexpr int B_DRAIN = B_OFIN + 2;     // abort path: MMAs in flight
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort word
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -191,10 +198,13 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::B_VFULL + s), 1);
       mbar_init(bar(C::B_VEMPTY + s), 1);
     }
-    for (int x = 0; x < C::NSB; ++x) mbar_init(bar(C::B_SFULL + x), 1);
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < C::NSB; ++x) {
+      mbar_init(bar(C::B_SFULL + x), 1);
       mbar_init(bar(C::B_PFULL + x), 4);  // one arrival per softmax warp of the tile
+    }
+    for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::B_ODONE + x), 1);
+      mbar_init(bar(C::B_OFIN + x), 1);
     }
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -333,7 +343,8 @@ __global__ void __launch_bounds__(384, 1)
         // before (number n - 3), and the tensor pipe runs in issue order, so
         // that P is read before it is overwritten; the softmax of a tile finds
         // its next S computed while it works on the current one.
-        auto sbuf = [&](int x, int j) { return (min(j + x, nA) + min(j, nB)) % 3; };
+        auto snum = [&](int x, int j) { return min(j + x, nA) + min(j, nB); };
+        auto sbuf = [&](int x, int j) { return snum(x, j) % 3; };
         int k_waited = 0;  // K tiles waited for (first uses come in order)
         auto s3 = [&](int x, int j) -> bool {
           if (j >= k_waited) {
@@ -349,7 +360,8 @@ __global__ void __launch_bounds__(384, 1)
           if ((x == 0 || j >= nA) &&
               !mbar_wait(bar(C::B_VFULL + st), (j / C::NS) & 1, abort_flag, p.err, kErrTimeoutMma))
             return false;
-          if (!mbar_wait(bar(C::B_PFULL + x), j & 1, abort_flag, p.err, kErrTimeoutMma))
+          if (!mbar_wait(bar(C::B_PFULL + sbuf(x, j)), (snum(x, j) / 3) & 1, abort_flag, p.err,
+                         kErrTimeoutMma))
             return false;
           tc_fence_after();
           const uint64_t vd = desc_add(v_desc, st * C::TILE);
@@ -363,6 +375,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int kk = 1; kk < 8; ++kk)
             mma_ts_k<ID_O, 1>(od, pa + kk * 8, desc_add(vd, kk * 2048));
           mma_commit(bar(C::B_ODONE + x));
+          if (j == nx[x] - 1) mma_commit(bar(C::B_OFIN + x));
           if (x == 1 || j >= nB) mma_commit(bar(C::B_VEMPTY + st));  // V_j's last use
           return true;
         };
@@ -547,12 +560,14 @@ __global__ void __launch_bounds__(384, 1)
       l = l * alpha + sum;
       // O holds P_0..P_{j-1} contributions; it must be final before it is
       // rescaled.  The S just waited for was issued, by the same thread,
-      // after O += P_x(j-1) V (with ROT3 after the P V that read its buffer
-      // before), and a commit tracks every earlier tcgen05 operation of its
+      // after the P V that read its buffer before (without ROT3, O += P_x(j-1)
+      // V), and a commit tracks every earlier tcgen05 operation of its
       // thread, so that product has completed and P_x(j) may overwrite the
-      // columns it read; the wait below is kept for the rescale alone and
-      // returns at once.  (O += P_x(j) V waits for this tile's P, so the
-      // barrier is never two phases ahead of a waiter.)
+      // columns it read.  The wait below is for the rescale: without ROT3 it
+      // returns at once; with ROT3 the S implies only O += P_x(j-2) V, and it
+      // waits for O += P_x(j-1) V.  Either way the barrier has completed the
+      // phase before the one waited for, and O += P_x(j) V waits for this
+      // tile's P, so it is never two phases from the waiter.
       const bool resc = j > 0 && __any_sync(0xffffffffu, upd);
       if (resc) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (j - 1) & 1, abort_flag,
@@ -573,12 +588,20 @@ __global__ void __launch_bounds__(384, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(bar(C::B_PFULL + x));
+      mbar_arrive_warp(bar(C::B_PFULL + sb));
     }
     // ------------------------------------------------------------ epilogue
+    // With ROT3 the per-tile P V barrier can be two phases behind here (the
+    // last S waited for implies only O += P_x(nt-3) V), so the epilogue waits
+    // for the barrier committed once after the tile's last P V.  Without
+    // ROT3 that S implies O += P_x(nt-2) V, and the per-tile barrier is at
+    // most one phase behind.
     if (ok && nt > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + x), (nt - 1) & 1, abort_flag,
-                                             p.err, kErrTimeoutEpilogue));
+      ok = __all_sync(0xffffffffu,
+                      C::ROT3 ? mbar_wait(bar(C::B_OFIN + x), 0, abort_flag, p.err,
+                                          kErrTimeoutEpilogue)
+                              : mbar_wait(bar(C::B_ODONE + x), (nt - 1) & 1, abort_flag, p.err,
+                                          kErrTimeoutEpilogue));
     if (ok && nt > 0) {
       tc_fence_after();
       const float inv_l = p.o_scale / l;

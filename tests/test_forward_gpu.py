@@ -342,6 +342,21 @@ def test_cta_pair_forward_equals_the_two_tile_forward(tile_rows, N, causal):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("d", [64, 96, 256])
+def test_pair_setting_gives_the_two_tile_result_at_other_head_dims(tile_rows, d):
+    """The pair of CTAs exists at d = 128 only; elsewhere 512 rows per CTA
+    acts as 256 (at d = 256, where only the one-tile kernel exists, both
+    settings run it), so the outputs are the same bits."""
+    inp = make_inputs(1, 4, 2, 1000, d, seed=9000 + d)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    tile_rows(256)
+    o1, l1 = nan_forward(q, k, v, causal=True)
+    tile_rows(512)
+    o2, l2 = nan_forward(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_cta_pair_forward_with_query_offset(tile_rows):
     import exact_attention_27_gb300 as fa
     tile_rows(512)
