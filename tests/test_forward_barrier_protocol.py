@@ -1,5 +1,5 @@
-"""The barrier protocol of the d = 64 two-tile forward (fa_fwd.cu), checked on
-a model under random interleavings (host only, no GPU).
+"""The barrier protocols of the two-tile forward (fa_fwd.cu), checked on a
+model under random interleavings (host only, no GPU).
 
 At d = 64 three S buffers of tensor memory rotate between the CTA's two
 query tiles A and B (the n-th S issued goes to buffer n % 3, P is written
@@ -20,6 +20,11 @@ epilogue every product before them.  The same model with the former
 per-tile P barrier and per-tile epilogue wait finds both failures, which
 is why the kernel has one P barrier per S buffer and a barrier committed
 once after each tile's last P V.
+
+At d = 96 and 128 (and in the FP8 forward) each tile has its own S
+buffer and the order is S_A(0) S_B(0), then per key tile j: O_A += P_A V_j,
+S_A(j+1), O_B += P_B V_j, S_B(j+1).  There a tile's next S follows its own
+P V, so per-tile barriers suffice; the second model checks that too.
 """
 
 import random
@@ -167,6 +172,102 @@ def _outcomes(per_buffer_p, final_barrier, seed, tries=60):
                     r = str(e)
                 seen[r] = seen.get(r, 0) + 1
     return seen
+
+
+def _run_ping_pong(nA, nB, rng, stages=2):
+    """The d = 96 / 128 order: per-tile S buffer, P barrier and P V barrier."""
+    n_kv = max(nA, nB)
+    bars = {}
+
+    def bar(name):
+        return bars.setdefault(name, _Barrier())
+
+    issued_s = {0: 0, 1: 0}
+    p_written = [0, 0]
+    pv_done = [0, 0]
+
+    def producer():
+        for j in range(n_kv):
+            st, ph = j % stages, ((j // stages) - 1) & 1
+            if j >= stages:
+                yield ("KEMPTY", st), ph
+            bar(("KFULL", st)).arrive()
+            if j >= stages:
+                yield ("VEMPTY", st), ph
+            bar(("VFULL", st)).arrive()
+
+    def issuer():
+        def s(x, j):
+            issued_s[x] += 1
+            bar(("SFULL", x)).arrive()
+
+        if n_kv > 0:
+            yield ("KFULL", 0), 0
+            if nA > 0:
+                s(0, 0)
+            if nB > 0:
+                s(1, 0)
+            bar(("KEMPTY", 0)).arrive()
+        for j in range(n_kv):
+            st = j % stages
+            yield ("VFULL", st), (j // stages) & 1
+            k_ready = False
+            for x in (0, 1):
+                if j >= (nA, nB)[x]:
+                    continue
+                yield ("PFULL", x), j & 1
+                _check(p_written[x] == j + 1, "P of another step")
+                pv_done[x] += 1
+                bar(("ODONE", x)).arrive()
+                if j + 1 < n_kv and j + 1 < (nA, nB)[x]:
+                    if not k_ready:
+                        yield ("KFULL", (j + 1) % stages), ((j + 1) // stages) & 1
+                        k_ready = True
+                    s(x, j + 1)
+            bar(("VEMPTY", st)).arrive()
+            if k_ready:
+                bar(("KEMPTY", (j + 1) % stages)).arrive()
+
+    def softmax(x):
+        nt = (nA, nB)[x]
+        for j in range(nt):
+            yield ("SFULL", x), j & 1
+            _check(issued_s[x] == j + 1, "softmax read another step's S")
+            if j > 0 and rng.random() < 0.5:
+                yield ("ODONE", x), (j - 1) & 1
+                _check(pv_done[x] >= j, "O rescaled before its last P V")
+            p_written[x] += 1
+            bar(("PFULL", x)).arrive()
+        if nt > 0:
+            yield ("ODONE", x), (nt - 1) & 1
+            _check(pv_done[x] == nt, "epilogue before the last P V")
+
+    roles = {"producer": producer(), "issuer": issuer(), "A": softmax(0), "B": softmax(1)}
+    waiting = dict.fromkeys(roles)
+    alive = set(roles)
+    while alive:
+        ready = [r for r in alive if waiting[r] is None or bar(waiting[r][0]).passed(waiting[r][1])]
+        if not ready:
+            return "deadlock"
+        r = rng.choice(sorted(ready))
+        try:
+            waiting[r] = next(roles[r])
+        except StopIteration:
+            alive.discard(r)
+    return "ok"
+
+
+@pytest.mark.parametrize("seed", [5, 6])
+def test_ping_pong_order_is_safe_under_any_interleaving(seed):
+    rng = random.Random(seed)
+    for nA in range(8):
+        for nB in range(8):
+            for _ in range(60):
+                try:
+                    r = _run_ping_pong(nA, nB, rng)
+                except _Violation as e:
+                    r = str(e)
+                assert r == "ok", (nA, nB, r)
 
 
 @pytest.mark.parametrize("seed", [1, 2, 3])
