@@ -136,7 +136,7 @@ def test_preprocess_row_dot(d):
     import exact_attention_27_gb300 as fa
     inp = make_inputs(3, 5, 5, 333, d, seed=d, with_grad=True)
     o, do = inp["q"].cuda(), inp["do"].cuda()
-    D = torch.empty(o.shape[:-1], dtype=torch.float32, device="cuda")
+    D = torch.full(o.shape[:-1], float("nan"), dtype=torch.float32, device="cuda")
     fa.fa_backward_preprocess(o, do, D)
     torch.cuda.synchronize()
     ref = oracle.row_dot(as_f64(inp["do"]), as_f64(inp["q"]))
