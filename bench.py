@@ -156,6 +156,26 @@ def _rotation(bytes_per_set):
     return max(1, math.ceil(3 * L2_BYTES / bytes_per_set))
 
 
+def step_set_bytes(w):
+    """Device bytes of one step's buffers: q, k, v, dO in; o, L, dq, dk, dv out."""
+    q = w.B * w.Hq * w.N * w.d * 2    # q, dO, o, dq
+    kv = w.B * w.Hkv * w.N * w.d * 2  # k, v, dk, dv
+    return 4 * q + 4 * kv + w.B * w.Hq * w.N * 4
+
+
+def bench_config(w, world):
+    """The benchmark configuration, the same dict in both arms' lines: the
+    workload, how it runs across GPUs, and how the device arm keeps a step's
+    inputs out of L2 (the reference arm runs on the host and times the
+    same workload)."""
+    set_bytes = step_set_bytes(w)
+    return {"workload": w.describe(), "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "N": w.N,
+            "d": w.d, "causal": True,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": f"inputs larger than L2: {_rotation(set_bytes)} rotating input sets of "
+                  f"{set_bytes / 2**20:.0f} MiB, steps back to back"}
+
+
 def run_ours(args, rank, world):
     import torch
     import exact_attention_27_gb300 as fa
@@ -182,6 +202,7 @@ def run_ours(args, rank, world):
 
     first = new_set()
     set_bytes = sum(x.numel() * x.element_size() for x in first.values())
+    assert set_bytes == step_set_bytes(w)
     R = _rotation(set_bytes)
     sets = [first] + [new_set() for _ in range(R - 1)]
     flops_fwd, flops_bwd = w.fwd_flops(), w.bwd_flops()
@@ -264,12 +285,9 @@ def run_ours(args, rank, world):
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.describe(), "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "N": w.N,
-                   "d": w.d, "causal": True, "step": "fa_forward + fa_backward",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"inputs larger than L2: {R} rotating input sets of "
-                         f"{set_bytes / 2**20:.0f} MiB, steps back to back",
-                   "frac_of_peak": round(value / world / tflops_peak, 4)},
+        "config": bench_config(w, world),
+        "step": "fa_forward + fa_backward",
+        "frac_of_peak": round(value / world / tflops_peak, 4),
         "fwd_ms": round(fwd_avg, 5),
         "bwd_ms": round(ms_per_step - fwd_avg, 5),
         "bwd_main_kernel_ms": round(bwd_main_avg, 5),
@@ -311,7 +329,7 @@ def summary(result):
     last key of the line so that a reader that keeps only the end of the
     output still sees them: [workload, ms, TFLOP/s, fraction of peak]."""
     rows = [["step: " + result["config"]["workload"], result["ms_per_step"], result["value"],
-             result["config"]["frac_of_peak"]],
+             result["frac_of_peak"]],
             ["bwd main kernel (roofline)", result["bwd_main_kernel_ms"],
              result["roofline"]["achieved"], result["roofline"]["frac"]]]
     for key in ("fwd_workloads", "bwd_workloads"):
@@ -890,8 +908,8 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.describe(), "B": w.B, "H_q": w.Hq, "H_kv": w.Hkv, "N": w.N,
-                   "d": w.d, "causal": True, "step": "oracle forward + backward"},
+        "config": bench_config(w, world),
+        "step": "oracle forward + backward",
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
