@@ -455,21 +455,36 @@ def run_forward_only(args):
     _build.build()
     w = WORKLOADS[args.forward_only]
     inp = make_inputs(w.B, w.Hq, w.Hkv, w.N, w.d, seed=7)
-    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    o = torch.empty_like(q)
+    if args.fp8:  # the e4m3 forward on the same shape (d = 128), unit descales
+        if w.d != 128:
+            raise SystemExit("--fp8 needs a d = 128 workload")
+        q = inp["q"].to(torch.float8_e4m3fn).cuda()
+        k = inp["k"].to(torch.float8_e4m3fn).cuda()
+        v = inp["v"].to(torch.float8_e4m3fn).transpose(-1, -2).contiguous().cuda()
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+
+        def launch():
+            fa.fa_forward_fp8(q, k, v, o, lse, w.scale, w.causal)
+    else:
+        q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+
+        def launch():
+            fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device="cuda")
     for _ in range(args.warmup):
-        fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
+        launch()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record()
     for _ in range(args.steps):
-        fa.fa_forward(q, k, v, o, lse, w.scale, w.causal)
+        launch()
     e.record()
     torch.cuda.synchronize()
     if fa.fa_last_device_error() != 0:
         raise RuntimeError("device error")
     ms = s.elapsed_time(e) / args.steps
-    return {"workload": w.describe(), "launches": args.warmup + args.steps, "ms": round(ms, 4),
+    return {"workload": w.describe() + (" e4m3" if args.fp8 else ""),
+            "launches": args.warmup + args.steps, "ms": round(ms, 4),
             "tflops": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1)}
 
 
@@ -929,6 +944,8 @@ def main():
                     help="time the step only (no extra workloads, e2e or CPU baseline)")
     ap.add_argument("--forward-only", choices=sorted(WORKLOADS), default=None,
                     help="run fa_forward alone on one workload (for kernel profiles)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="with --forward-only: the e4m3 forward (d = 128 workloads)")
     ap.add_argument("--backward-only", choices=sorted(BWD_NAMES), default=None,
                     help="run fa_backward alone on one backward workload (for kernel profiles)")
     ap.add_argument("--sweep-tile-rows", action="store_true",
