@@ -36,7 +36,11 @@
 // dP [320,384).
 // Shared memory: K, V (64 x 256 bf16, 32 KB each), Q, dO (128 x 256 bf16,
 // 64 KB each), P, dS (128 x 64 bf16, 16 KB each) = 224 KB.  One stage of
-// each: at 128 rows of 512 bytes, a second Q/dO stage does not fit.
+// each: at 128 rows of 512 bytes, a second Q/dO stage does not fit.  So Q
+// and dO are split into two halves of d (128 columns) with a barrier each:
+// the MMA issuer starts a product on half 0 while half 1 is still landing,
+// and the producer reloads a half as soon as the dV^T / dK^T products that
+// read it are done, rather than after both halves are.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -66,20 +70,23 @@ struct Kv256Cfg {
   static constexpr int OFF_P = OFF_DO + QTILE;
   static constexpr int OFF_DS = OFF_P + PBYTES;
   static constexpr int OFF_BAR = OFF_DS + PBYTES;
+  // Q and dO are handled as two halves of d (128 columns, 32 KB each), so
+  // that each half is reloaded as soon as the products reading it are done.
   static constexpr int B_KV = 0;
-  static constexpr int B_QFULL = 1;
-  static constexpr int B_DOFULL = 2;
-  static constexpr int B_QEMPTY = 3;     // dK^T of the step done: Q free
-  static constexpr int B_DOEMPTY = 4;    // dV^T of the step done: dO free
-  static constexpr int B_S = 5;          // S in tensor memory
-  static constexpr int B_DP = 6;         // dP in tensor memory
-  static constexpr int B_P = 7;          // P in shared memory, S read (8 warp arrivals)
-  static constexpr int B_DS = 8;         // dS in shared memory, dP read (8 warp arrivals)
-  static constexpr int B_PFREE = 9;      // dV^T done: P buffer free
-  static constexpr int B_DSFREE = 10;    // dK^T done: dS buffer free
-  static constexpr int B_FINAL = 11;     // every product issued has completed (once)
-  static constexpr int B_DRAIN = 12;
-  static constexpr int NBAR = 13;
+  static constexpr int B_QFULL = 1;      // [2] Q half landed
+  static constexpr int B_DOFULL = 3;     // [2]
+  static constexpr int B_QEMPTY = 5;     // [2] dK^T[h] of the step done: Q half h free
+  static constexpr int B_DOEMPTY = 7;    // [2] dV^T[h] of the step done: dO half h free
+  static constexpr int B_S = 9;          // S in tensor memory
+  static constexpr int B_DP = 10;        // dP in tensor memory
+  static constexpr int B_P = 11;         // P in shared memory, S read (8 warp arrivals)
+  static constexpr int B_DS = 12;        // dS in shared memory, dP read (8 warp arrivals)
+  static constexpr int B_PFREE = 13;     // dV^T done: P buffer free
+  static constexpr int B_DSFREE = 14;    // dK^T done: dS buffer free
+  static constexpr int B_FINAL = 15;     // every product issued has completed (once)
+  static constexpr int B_DRAIN = 16;
+  static constexpr int NBAR = 17;
+  static constexpr int QHALF = 2 * QSUB;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 320;
@@ -170,14 +177,18 @@ __global__ void __launch_bounds__(320, 1)
     if (n_steps > 0) {
       int bhq, it;
       step_coords(0, bhq, it);
-      mbar_arrive_expect_tx(bar(C::B_DOFULL), C::QTILE);
-      mbar_arrive_expect_tx(bar(C::B_QFULL), C::QTILE);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tma_load_3d(sdO + c * C::QSUB, &tmdO, bar(C::B_DOFULL), 64 * c, it * C::BQ, bhq);
+      for (int h = 0; h < 2; ++h) {
+        mbar_arrive_expect_tx(bar(C::B_DOFULL + h), C::QHALF);
+        for (int c = 2 * h; c < 2 * h + 2; ++c)
+          tma_load_3d(sdO + c * C::QSUB, &tmdO, bar(C::B_DOFULL + h), 64 * c, it * C::BQ, bhq);
+      }
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tma_load_3d(sQ + c * C::QSUB, &tmQ, bar(C::B_QFULL), 64 * c, it * C::BQ, bhq);
+      for (int h = 0; h < 2; ++h) {
+        mbar_arrive_expect_tx(bar(C::B_QFULL + h), C::QHALF);
+        for (int c = 2 * h; c < 2 * h + 2; ++c)
+          tma_load_3d(sQ + c * C::QSUB, &tmQ, bar(C::B_QFULL + h), 64 * c, it * C::BQ, bhq);
+      }
     }
   }
   if (warp == 9) {
@@ -194,27 +205,44 @@ __global__ void __launch_bounds__(320, 1)
     if (elect_one()) {
       // dO of step s once dV^T of step s - 1 has read its buffer, then Q once
       // dK^T has; step 0 was issued before the CTA barrier.
-      int do_issued = n_steps > 0 ? 1 : 0, q_issued = do_issued;
+      int do_half[2], q_half[2];  // steps whose half h was issued
+      do_half[0] = do_half[1] = q_half[0] = q_half[1] = n_steps > 0 ? 1 : 0;
       for (int s = 1; s < n_steps; ++s) {
         int bhq, it;
         step_coords(s, bhq, it);
-        if (!mbar_wait(bar(C::B_DOEMPTY), (s - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
-        mbar_arrive_expect_tx(bar(C::B_DOFULL), C::QTILE);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tma_load_3d(sdO + c * C::QSUB, &tmdO, bar(C::B_DOFULL), 64 * c, it * C::BQ, bhq);
-        do_issued = s + 1;
-        if (!mbar_wait(bar(C::B_QEMPTY), (s - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) break;
-        mbar_arrive_expect_tx(bar(C::B_QFULL), C::QTILE);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tma_load_3d(sQ + c * C::QSUB, &tmQ, bar(C::B_QFULL), 64 * c, it * C::BQ, bhq);
-        q_issued = s + 1;
+        // Halves in the order the products free them: dO[0], dO[1] (dV^T),
+        // then Q[0], Q[1] (dK^T).
+        bool go = true;
+#pragma unroll 1
+        for (int h = 0; h < 2 && go; ++h) {
+          if (!mbar_wait(bar(C::B_DOEMPTY + h), (s - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) {
+            go = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::B_DOFULL + h), C::QHALF);
+          for (int c = 2 * h; c < 2 * h + 2; ++c)
+            tma_load_3d(sdO + c * C::QSUB, &tmdO, bar(C::B_DOFULL + h), 64 * c, it * C::BQ, bhq);
+          do_half[h] = s + 1;
+        }
+#pragma unroll 1
+        for (int h = 0; h < 2 && go; ++h) {
+          if (!mbar_wait(bar(C::B_QEMPTY + h), (s - 1) & 1, abort_flag, p.err, kErrTimeoutLoad)) {
+            go = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::B_QFULL + h), C::QHALF);
+          for (int c = 2 * h; c < 2 * h + 2; ++c)
+            tma_load_3d(sQ + c * C::QSUB, &tmQ, bar(C::B_QFULL + h), 64 * c, it * C::BQ, bhq);
+          q_half[h] = s + 1;
+        }
+        if (!go) break;
       }
       if (*abort_flag) {
         mbar_wait_timed(bar(C::B_KV), 0);
-        if (do_issued > 0) mbar_wait_timed(bar(C::B_DOFULL), (do_issued - 1) & 1);
-        if (q_issued > 0) mbar_wait_timed(bar(C::B_QFULL), (q_issued - 1) & 1);
+        for (int h = 0; h < 2; ++h) {
+          if (do_half[h] > 0) mbar_wait_timed(bar(C::B_DOFULL + h), (do_half[h] - 1) & 1);
+          if (q_half[h] > 0) mbar_wait_timed(bar(C::B_QFULL + h), (q_half[h] - 1) & 1);
+        }
       }
     }
   } else if (warp == 9) {
@@ -239,7 +267,14 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         mma_ss_k<ID_SP, 0>(tmem + C::COL_DP, do_k, v_k);
 #pragma unroll
-        for (int kk = 1; kk < 16; ++kk)
+        for (int kk = 1; kk < 8; ++kk)
+          mma_ss_k<ID_SP, 1>(tmem + C::COL_DP,
+                             desc_add(do_k, (kk >> 2) * C::QSUB + (kk & 3) * 32),
+                             desc_add(v_k, (kk >> 2) * C::KSUB + (kk & 3) * 32));
+        if (!mbar_wait(bar(C::B_DOFULL + 1), ph, abort_flag, p.err, kErrTimeoutMma)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 8; kk < 16; ++kk)
           mma_ss_k<ID_SP, 1>(tmem + C::COL_DP,
                              desc_add(do_k, (kk >> 2) * C::QSUB + (kk & 3) * 32),
                              desc_add(v_k, (kk >> 2) * C::KSUB + (kk & 3) * 32));
@@ -249,7 +284,14 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         mma_ss_k<ID_SP, 0>(tmem + C::COL_S, q_k, k_k);
 #pragma unroll
-        for (int kk = 1; kk < 16; ++kk)
+        for (int kk = 1; kk < 8; ++kk)
+          mma_ss_k<ID_SP, 1>(tmem + C::COL_S,
+                             desc_add(q_k, (kk >> 2) * C::QSUB + (kk & 3) * 32),
+                             desc_add(k_k, (kk >> 2) * C::KSUB + (kk & 3) * 32));
+        if (!mbar_wait(bar(C::B_QFULL + 1), ph, abort_flag, p.err, kErrTimeoutMma)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 8; kk < 16; ++kk)
           mma_ss_k<ID_SP, 1>(tmem + C::COL_S,
                              desc_add(q_k, (kk >> 2) * C::QSUB + (kk & 3) * 32),
                              desc_add(k_k, (kk >> 2) * C::KSUB + (kk & 3) * 32));
@@ -268,8 +310,8 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int kq = 1; kq < 8; ++kq)
             mma_ss_k<ID_T, 1>(dst, desc_add(a, kq * 2048), desc_add(p_mn, kq * 2048));
+          mma_commit(bar(C::B_DOEMPTY + h));  // dO half h is no longer read
         }
-        mma_commit(bar(C::B_DOEMPTY));
         mma_commit(bar(C::B_PFREE));
         // dK^T[h] += Q^T[h] dS
         if (!mbar_wait(bar(C::B_DS), ph, abort_flag, p.err, kErrTimeoutMma)) break;
@@ -285,8 +327,8 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int kq = 1; kq < 8; ++kq)
             mma_ss_k<ID_T, 1>(dst, desc_add(a, kq * 2048), desc_add(ds_mn, kq * 2048));
+          mma_commit(bar(C::B_QEMPTY + h));  // Q half h is no longer read
         }
-        mma_commit(bar(C::B_QEMPTY));
         mma_commit(bar(C::B_DSFREE));
         if (s == n_steps - 1) mma_commit(bar(C::B_FINAL));
       }
