@@ -451,20 +451,22 @@ __global__ void __launch_bounds__(384, 1)
       ++wg_phase;
       return __all_sync(0xffffffffu, r);
     };
-    // -L log2e and -D of query row t of step s (negated, so that the loop
-    // below adds them; dead rows: -L = -inf so P = 0).  Each step's values
-    // are loaded one step ahead, so that the global-load latency is not on
-    // the step's critical path.
-    auto load_ld = [&](int s, float& lv, float& dv) {
+    // L and D of query row t of step s, loaded one step ahead from an index
+    // that is always valid (row 0 for rows past N), and left as loaded until
+    // the next step stores -L log2e and -D (negated, so that the loop below
+    // adds them; dead rows: -L = -inf so P = 0).  Nothing then waits for the
+    // loads within the step that issues them.
+    auto load_ld = [&](int s, float& lv, float& dv, bool& live) {
       const int g = s / per_head;
       const int qrow = (i0 + (s - g * per_head)) * C::BQ + t;
-      const bool live = qrow < p.N;
+      live = qrow < p.N;
       const size_t idx = static_cast<size_t>(b * p.Hq + hkv * p.G + g) * p.N + (live ? qrow : 0);
-      lv = live ? -p.lse[idx] * kLog2e : -INFINITY;
-      dv = live ? -p.Dvec[idx] : 0.0f;
+      lv = p.lse[idx];
+      dv = p.Dvec[idx];
     };
     float l_cur = 0.0f, d_cur = 0.0f;
-    if (n_steps > 0) load_ld(0, l_cur, d_cur);
+    bool live_cur = false;
+    if (n_steps > 0) load_ld(0, l_cur, d_cur, live_cur);
     // Step s + 1's dS^T overwrites step s's in shared memory: it is written
     // once dP^T of step s + 1 is in, which is computed only after the drain
     // has taken step s's dQ, so every product of step s (the ones reading
@@ -474,9 +476,9 @@ __global__ void __launch_bounds__(384, 1)
       const int it = i0 + (s - g * per_head);
       const int q0 = it * C::BQ;
       const int buf = s & 1;
-      sL[buf * 128 + t] = l_cur;
-      sD[buf * 128 + t] = d_cur;
-      if (s + 1 < n_steps) load_ld(s + 1, l_cur, d_cur);  // used at the next step
+      sL[buf * 128 + t] = live_cur ? -l_cur * kLog2e : -INFINITY;
+      sD[buf * 128 + t] = live_cur ? -d_cur : 0.0f;
+      if (s + 1 < n_steps) load_ld(s + 1, l_cur, d_cur, live_cur);  // used at the next step
       if (!(ok = wg_sync())) break;
       ok = __all_sync(0xffffffffu,
                       mbar_wait(bar(C::B_S), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));

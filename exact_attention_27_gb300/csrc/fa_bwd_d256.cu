@@ -346,26 +346,31 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const int kbase = jt * C::BK + 32 * g;  // first key of this warp's half of the tile
     const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
-    // -L log2e and -D of this thread's row at step s (dead rows: P = 0).
-    auto load_ld = [&](int s, float& nl, float& nd) {
+    // L and D of this thread's row at step s, loaded one step ahead from an
+    // index that is always valid and left as loaded until the step that uses
+    // them forms -L log2e and -D (dead rows: -L = -inf so P = 0).
+    auto load_ld = [&](int s, float& l, float& dd, bool& live) {
       int bhq, it;
       step_coords(s, bhq, it);
       const int q = it * C::BQ + row;
-      const bool live = q < p.N;
+      live = q < p.N;
       const size_t idx = static_cast<size_t>(bhq) * p.N + (live ? q : 0);
-      nl = live ? -p.lse[idx] * kLog2e : -INFINITY;
-      nd = live ? -p.Dvec[idx] : 0.0f;
+      l = p.lse[idx];
+      dd = p.Dvec[idx];
     };
-    float nl_cur = 0.0f, nd_cur = 0.0f;
-    if (n_steps > 0) load_ld(0, nl_cur, nd_cur);
+    float l_cur = 0.0f, d_cur = 0.0f;
+    bool live_cur = false;
+    if (n_steps > 0) load_ld(0, l_cur, d_cur, live_cur);
     bool ok = true;
     for (int s = 0; s < n_steps; ++s) {
       const uint32_t ph = s & 1;
       int bhq, it;
       step_coords(s, bhq, it);
       const int q = it * C::BQ + row;
+      const float nl_cur = live_cur ? -l_cur * kLog2e : -INFINITY;
+      const float nd_cur = live_cur ? -d_cur : 0.0f;
       const uint64_t nl2 = f2_pack(nl_cur, nl_cur), nd2 = f2_pack(nd_cur, nd_cur);
-      if (s + 1 < n_steps) load_ld(s + 1, nl_cur, nd_cur);  // used at the next step
+      if (s + 1 < n_steps) load_ld(s + 1, l_cur, d_cur, live_cur);  // used at the next step
       ok = __all_sync(0xffffffffu,
                       mbar_wait(bar(C::B_S), ph, abort_flag, p.err, kErrTimeoutSoftmax));
       if (!ok) break;

@@ -480,21 +480,25 @@ __global__ void __launch_bounds__(448, 1)
       ++wg_phase;
       return __all_sync(0xffffffffu, r);
     };
-    // -L*log2e and -D of half h into ring slot h % NLD: thread t < 64 loads L
-    // of query t of the half, t >= 64 loads D of query t - 64 (negated, so the
-    // compute warps add them).  Rows past N get -L = -inf (so P = 0), D = 0.
+    // L and D of half h: thread t < 64 loads L of query t of the half, t >= 64
+    // D of query t - 64.  Rows past N read as L = +inf (so P = 0) and D = -0.
+    // The raw value is kept until it is stored, so that nothing waits for the
+    // load before then: the loads for tile s + 3 are in flight while tile s's
+    // dQ is drained.
     auto load_ld = [&](int h) -> float {
       if (h >= n_half) return 0.0f;
       int bhq, it;
       step_coords(h >> 1, bhq, it);
       const int qrow = it * C::BQ + (h & 1) * 64 + (t & 63);
-      if (qrow >= p.N) return t < 64 ? -INFINITY : 0.0f;  // dead rows: P = 0
+      if (qrow >= p.N) return t < 64 ? INFINITY : -0.0f;
       const size_t idx = static_cast<size_t>(bhq) * p.N + qrow;
-      return t < 64 ? -p.lse[idx] * kLog2e : -p.Dvec[idx];
+      return t < 64 ? p.lse[idx] : p.Dvec[idx];
     };
-    auto store_ld = [&](int h, float val) {
+    // Ring slot h % NLD takes -L log2e and -D (negated, so the compute warps add them).
+    auto store_ld = [&](int h, float raw) {
       if (h >= n_half) return;
-      reinterpret_cast<float*>(smem + C::OFF_LD)[(h % C::NLD) * 128 + t] = val;
+      reinterpret_cast<float*>(smem + C::OFF_LD)[(h % C::NLD) * 128 + t] =
+          t < 64 ? -raw * kLog2e : -raw;
       mbar_arrive_warp(bar(C::B_LDFULL + h % C::NLD));
     };
     // This warpgroup alone reads what the row-dot pass (the grid before this
