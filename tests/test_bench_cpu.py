@@ -53,3 +53,24 @@ def test_errors_vanish_against_the_oracle_itself_and_catch_a_wrong_dk():
 
 def test_median_and_min():
     assert bench._med_min([3.0, 1.0, 2.0]) == {"median": 2.0, "min": 1.0}
+
+
+def test_reference_arm_line_carries_the_contract_keys_and_the_same_config():
+    """The reference arm (the oracle on the host cores) prints the keys the
+    benchmark line needs, and its `config` is the dict the device arm prints
+    for the same workload, so the two lines compare as the same config."""
+    import json
+    args = types.SimpleNamespace(steps=1, warmup=3)
+    line = bench.run_reference(args, rank=0, world=1)
+    json.dumps(line)
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["metric"] == bench.METRIC and line["unit"] == "TFLOP/s"
+    w = bench.WORKLOADS[bench.STEP_WORKLOAD]
+    assert line["config"] == bench.bench_config(w, 1)
+    assert line["config"]["workload"] == w.describe()
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert bench.bench_config(w, 2)["parallelism"] == "replicas x2"
