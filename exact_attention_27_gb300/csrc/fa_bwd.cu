@@ -97,10 +97,13 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float4* __restri
 // dK and dV kept on chip, dQ added to global memory).  Keys sit on the 128
 // TMEM lanes, so each softmax thread owns one key row.  Per query tile i:
 //
-//   S^T  = K_j Q_i^T                  tcgen05.mma, A and B K-major in smem
-//   dP^T = V_j dO_i^T                 tcgen05.mma
-//   P^T  = exp2(S^T scale log2e - L_i log2e)      threads, L_i saved by the forward
-//   dS^T = P^T o (dP^T - D_i)                     threads, D_i from B1
+//   S^T  = K_j Q_i^T - L_i / scale    tcgen05.mma, A and B K-major in smem;
+//                                     L_i (saved by the forward) enters as one
+//                                     more k-step: A = ones, B = -L_i / scale
+//                                     as three bf16 terms per query
+//   dP^T = V_j dO_i^T - D_i           tcgen05.mma, D_i (from B1) the same way
+//   P^T  = exp2(S^T scale log2e)                  threads
+//   dS^T = P^T o dP^T                             threads
 //   dV  += P^T dO_i                   tcgen05.mma, A = P^T (bf16) from TMEM
 //   dK  += dS^T Q_i                   tcgen05.mma, A = dS^T (bf16, K-major smem)
 //   dQ_i = dS K_j                     tcgen05.mma, A = the same dS^T buffer read
@@ -108,7 +111,8 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float4* __restri
 //                                     into the fp32 dQ accumulator
 // dK is multiplied by scale once at the end; dQ gets its scale in B3.
 //
-// Warp roles (384 threads): warps 0-3 key rows (P^T, dS^T, L/D, epilogue),
+// Warp roles (384 threads): warps 0-3 key rows (P^T, dS^T, the next step's
+// -L/scale and -D rows of the extra k-step, epilogue),
 // warps 4-7 dQ drain, warp 8 TMA, warp 9 MMA, warps 10-11 idle.  The drain
 // warpgroup takes a step's dQ out of TMEM at once (freeing the columns for
 // the next dP^T) and reduces it while the key-row warps go on to the next
@@ -140,8 +144,12 @@ struct BwdCfg {
   static constexpr int OFF_DO = OFF_Q + NQ * TILE;
   static constexpr int OFF_DS = OFF_DO + TILE;    // dS^T: 128 keys x 128 queries bf16
   static constexpr int OFF_STG = OFF_DS + 2 * SUB_BYTES;  // dQ staging: 4 x (32 rows x 32 fp32)
-  static constexpr int OFF_LD = OFF_STG + SUB_BYTES;     // -L log2e [2][128], -D [2][128]
-  static constexpr int OFF_BAR = OFF_LD + 4 * 128 * 4;
+  // Operands of S^T's and dP^T's last k-step: a 128 x 64 bf16 tile in the
+  // 128-byte swizzled layout whose 16-column slot 0 holds ones in columns
+  // 0-2 of every row (A, one row per key), slot 1 -L/scale and slot 2 -D of
+  // the step's queries as three bf16 terms each (B, one row per query).
+  static constexpr int OFF_AUG = OFF_STG + SUB_BYTES;
+  static constexpr int OFF_BAR = OFF_AUG + SUB_BYTES;
   static constexpr int B_KV = 0;
   static constexpr int B_QFULL = 1;               // [NQ]
   static constexpr int B_QEMPTY = B_QFULL + NQ;   // [NQ]
@@ -153,10 +161,10 @@ struct BwdCfg {
   static constexpr int B_DS = B_P + 1;            // dS^T in smem, dP^T read (128 arrivals)
   static constexpr int B_DQFULL = B_DS + 1;       // dQ in TMEM (dV, dP^T, dQ of the step done)
   static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ columns drained (128 arrivals)
-  static constexpr int B_WG = B_DQFREE + 1;      // key-row warpgroup sync (128 arrivals)
-  static constexpr int B_FINAL = B_WG + 1;        // every product issued has completed (once)
+  static constexpr int B_FINAL = B_DQFREE + 1;    // every product issued has completed (once)
   static constexpr int B_DRAIN = B_FINAL + 1;
-  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int B_AUG0 = B_DRAIN + 1;      // step 0's blocks written (128 arrivals)
+  static constexpr int NBAR = B_AUG0 + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 384;
@@ -229,8 +237,6 @@ __global__ void __launch_bounds__(384, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  float* sL = reinterpret_cast<float*>(smem + C::OFF_LD);        // [2][128]
-  float* sD = reinterpret_cast<float*>(smem + C::OFF_LD + 1024);  // [2][128]
 
   const int warp = threadIdx.x >> 5;
   const int kvz = blockIdx.x;  // flattened (batch, kv head)
@@ -271,9 +277,9 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar(C::B_DS), 128);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQFREE), 128);
-    mbar_init(bar(C::B_WG), 128);
     mbar_init(bar(C::B_FINAL), 1);
     mbar_init(bar(C::B_DRAIN), 1);
+    mbar_init(bar(C::B_AUG0), 128);
     *abort_flag = 0;
     fence_barrier_init();
     mbar_arrive_expect_tx(bar(C::B_KV), 2 * C::TILE);
@@ -349,7 +355,9 @@ __global__ void __launch_bounds__(384, 1)
         // columns of their accumulators are neither computed nor read.
         constexpr uint32_t id_kd = idesc_bf16_f32(128, D, false, true);  // dV, dK
         constexpr uint32_t id_q = idesc_bf16_f32(128, D, true, true);    // dQ
-        bool ok = mbar_wait(bar(C::B_KV), 0, abort_flag, p.err, kErrTimeoutMma);
+        bool ok = mbar_wait(bar(C::B_KV), 0, abort_flag, p.err, kErrTimeoutMma) &&
+                  mbar_wait(bar(C::B_AUG0), 0, abort_flag, p.err, kErrTimeoutMma);
+        const uint64_t aug_a = smem_desc_sw128(sbase + C::OFF_AUG, 16, 1024);  // ones, slot 0
         // S^T of step s (Q_s in stage s % NQ) into the S^T columns.
         auto issue_s = [&](int s) -> bool {
           const int qs = s % C::NQ;
@@ -363,6 +371,7 @@ __global__ void __launch_bounds__(384, 1)
             mma_ss(tmem + C::COL_S, smem_desc_sw128(sK + off, 16, 1024),
                    smem_desc_sw128(q_st + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
           }
+          mma_ss(tmem + C::COL_S, aug_a, desc_add(aug_a, 32), id_ss, 1u);  // - L / scale
           mma_commit(bar(C::B_S));
           return true;
         };
@@ -380,6 +389,7 @@ __global__ void __launch_bounds__(384, 1)
             mma_ss(tmem + C::COL_DP, smem_desc_sw128(sV + off, 16, 1024),
                    smem_desc_sw128(sdO + off, 16, 1024), id_ss, kk > 0 ? 1u : 0u);
           }
+          mma_ss(tmem + C::COL_DP, aug_a, desc_add(aug_a, 64), id_ss, 1u);  // - D
           mma_commit(bar(C::B_DP));
           return true;
         };
@@ -443,14 +453,7 @@ __global__ void __launch_bounds__(384, 1)
     const int key = jt * C::BK + t;
     const bool key_live = key < p.N;
     const float c = p.scale_log2;
-    uint32_t wg_phase = 0;
     bool ok = true;
-    auto wg_sync = [&]() -> bool {
-      mbar_arrive(bar(C::B_WG));
-      const bool r = mbar_wait(bar(C::B_WG), wg_phase & 1, abort_flag, p.err, kErrTimeoutSoftmax);
-      ++wg_phase;
-      return __all_sync(0xffffffffu, r);
-    };
     // L and D of query row t of step s, loaded one step ahead from an index
     // that is always valid (row 0 for rows past N), and left as loaded until
     // the next step stores -L log2e and -D (negated, so that the loop below
@@ -467,6 +470,30 @@ __global__ void __launch_bounds__(384, 1)
     float l_cur = 0.0f, d_cur = 0.0f;
     bool live_cur = false;
     if (n_steps > 0) load_ld(0, l_cur, d_cur, live_cur);
+    // Row t of the extra k-step's tile: v as hi + mid + lo (bf16) in
+    // columns 0-2 of 16-column slot `slot`.
+    const uint32_t sAug = sbase + C::OFF_AUG;
+    auto write_aug = [&](int slot, float v) {
+      float hi = v, mid = 0.0f, lo = 0.0f;
+      if (isfinite(v)) {
+        hi = __bfloat162float(__float2bfloat16_rn(v));
+        const float r1 = v - hi;
+        mid = __bfloat162float(__float2bfloat16_rn(r1));
+        lo = r1 - mid;
+      }
+      st_shared_v4(sAug + sw128(t, 2 * slot), pack_bf16x2(hi, mid), pack_bf16x2(lo, 0.0f), 0u,
+                   0u);
+      st_shared_v4(sAug + sw128(t, 2 * slot + 1), 0u, 0u, 0u, 0u);
+    };
+    // Ones in slot 0 (bf16 1.0 = 0x3f80) and step 0's -L/scale and -D.
+    st_shared_v4(sAug + sw128(t, 0), 0x3f803f80u, 0x3f80u, 0u, 0u);
+    st_shared_v4(sAug + sw128(t, 1), 0u, 0u, 0u, 0u);
+    if (n_steps > 0) {
+      write_aug(1, live_cur ? -__fdiv_rn(l_cur, p.scale) : -INFINITY);
+      write_aug(2, live_cur ? -d_cur : 0.0f);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(bar(C::B_AUG0));
     // Step s + 1's dS^T overwrites step s's in shared memory: it is written
     // once dP^T of step s + 1 is in, which is computed only after the drain
     // has taken step s's dQ, so every product of step s (the ones reading
@@ -475,17 +502,11 @@ __global__ void __launch_bounds__(384, 1)
       const int g = s / per_head;
       const int it = i0 + (s - g * per_head);
       const int q0 = it * C::BQ;
-      const int buf = s & 1;
-      sL[buf * 128 + t] = live_cur ? -l_cur * kLog2e : -INFINITY;
-      sD[buf * 128 + t] = live_cur ? -d_cur : 0.0f;
-      if (s + 1 < n_steps) load_ld(s + 1, l_cur, d_cur, live_cur);  // used at the next step
-      if (!(ok = wg_sync())) break;
+      if (s + 1 < n_steps) load_ld(s + 1, l_cur, d_cur, live_cur);  // written during this step
       ok = __all_sync(0xffffffffu,
                       mbar_wait(bar(C::B_S), s & 1, abort_flag, p.err, kErrTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
-      const float4* L4b = reinterpret_cast<const float4*>(sL + buf * 128);  // -L log2e
-      const float4* D4b = reinterpret_cast<const float4*>(sD + buf * 128);  // -D
       // Masking is needed only on the diagonal tile and for keys past N.
       const bool masked = __any_sync(0xffffffffu, (CAUSAL && it == jt) || !key_live);
       const uint64_t c2 = f2_pack(c, c);
@@ -510,15 +531,13 @@ __global__ void __launch_bounds__(384, 1)
           const uint32_t(&sv)[32] = sv2[cc & 1];
 #pragma unroll
           for (int u4 = 0; u4 < 8; ++u4) {
-            const float4 nl = L4b[cc * 8 + u4];
             float pv[4];
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(sv[4 * u4]), __uint_as_float(sv[4 * u4 + 1])),
+                             c2),
+                      pv[0], pv[1]);
             f2_unpack(
-                f2_fma(f2_pack(__uint_as_float(sv[4 * u4]), __uint_as_float(sv[4 * u4 + 1])), c2,
-                       f2_pack(nl.x, nl.y)),
-                pv[0], pv[1]);
-            f2_unpack(
-                f2_fma(f2_pack(__uint_as_float(sv[4 * u4 + 2]), __uint_as_float(sv[4 * u4 + 3])),
-                       c2, f2_pack(nl.z, nl.w)),
+                f2_mul(f2_pack(__uint_as_float(sv[4 * u4 + 2]), __uint_as_float(sv[4 * u4 + 3])),
+                       c2),
                 pv[2], pv[3]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) pv[e] = ex2_approx(pv[e]);
@@ -539,6 +558,11 @@ __global__ void __launch_bounds__(384, 1)
         p_pass(std::true_type{});
       else
         p_pass(std::false_type{});
+      // S^T of this step has been read: the next step's -L/scale goes into slot 1.
+      if (s + 1 < n_steps) {
+        write_aug(1, live_cur ? -__fdiv_rn(l_cur, p.scale) : -INFINITY);
+        fence_proxy_async_smem();
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::B_P));
@@ -560,22 +584,18 @@ __global__ void __launch_bounds__(384, 1)
           uint32_t dk16[16];
 #pragma unroll
           for (int u4 = 0; u4 < 8; ++u4) {
-            const float4 nd = D4b[cc * 8 + u4];
             const __nv_bfloat162 pa =
                 *reinterpret_cast<const __nv_bfloat162*>(&pk[cc * 16 + 2 * u4]);
             const __nv_bfloat162 pb =
                 *reinterpret_cast<const __nv_bfloat162*>(&pk[cc * 16 + 2 * u4 + 1]);
             const float2 p01 = __bfloat1622float2(pa);
             const float2 p23 = __bfloat1622float2(pb);
-            const uint64_t ds01 = f2_mul(
-                f2_pack(p01.x, p01.y),
-                f2_add(f2_pack(__uint_as_float(dpv[4 * u4]), __uint_as_float(dpv[4 * u4 + 1])),
-                       f2_pack(nd.x, nd.y)));
+            const uint64_t ds01 =
+                f2_mul(f2_pack(p01.x, p01.y),
+                       f2_pack(__uint_as_float(dpv[4 * u4]), __uint_as_float(dpv[4 * u4 + 1])));
             const uint64_t ds23 = f2_mul(
                 f2_pack(p23.x, p23.y),
-                f2_add(
-                    f2_pack(__uint_as_float(dpv[4 * u4 + 2]), __uint_as_float(dpv[4 * u4 + 3])),
-                    f2_pack(nd.z, nd.w)));
+                f2_pack(__uint_as_float(dpv[4 * u4 + 2]), __uint_as_float(dpv[4 * u4 + 3])));
             float dsv[4];
             f2_unpack(ds01, dsv[0], dsv[1]);
             f2_unpack(ds23, dsv[2], dsv[3]);
@@ -591,6 +611,8 @@ __global__ void __launch_bounds__(384, 1)
           if (cc + 1 < 4) tmem_wait_ld();
         }
       }
+      // dP^T of this step has been read: the next step's -D goes into slot 2.
+      if (s + 1 < n_steps) write_aug(2, live_cur ? -d_cur : 0.0f);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_DS));

@@ -24,9 +24,14 @@ Three hazards have no barrier of their own and rest on the issue order:
 S^T(s + 1) overwrites P^T(s) after dV(s) read it; dQ(s) overwrites dP^T(s)
 after the key rows read it (dQ waits for their dS^T); and the key rows
 write dS^T(s + 1) over dS^T(s) once dP^T(s + 1) is in, which was issued
-after dQ(s) and dK(s).  The model checks every read, and finds the three
-slips it should: dP^T(s + 1) issued without waiting for the drain, dK(s)
-issued after dP^T(s + 1), and dO released before dV has run.
+after dQ(s) and dK(s).  L and D enter S^T and dP^T as one more k-step whose
+B operand the key rows write for the next step: -L/scale once S^T(s) has
+completed and before they hand back P^T(s) (after which S^T(s + 1) is
+issued), -D once dP^T(s) has completed and before they hand back dS^T(s).
+The model checks every read, and finds the slips it should: dP^T(s + 1)
+issued without waiting for the drain, dK(s) issued after dP^T(s + 1), dO
+released before dV has run, and the next step's -L/scale written before
+S^T(s) has read the slot.
 """
 
 import random
@@ -52,7 +57,8 @@ class _Barrier:
 NQ = 2
 
 
-def _run(n_steps, rng, dq_free_wait=True, dk_before_dp=True, do_empty_after_dv=True):
+def _run(n_steps, rng, dq_free_wait=True, dk_before_dp=True, do_empty_after_dv=True,
+         aug_early=False):
     bars = {}
 
     def bar(name):
@@ -63,6 +69,8 @@ def _run(n_steps, rng, dq_free_wait=True, dk_before_dp=True, do_empty_after_dv=T
     ds_smem = [None]    # step of the dS^T tile
     q_stage = dict.fromkeys(range(NQ))
     do_stage = [None]
+    aug_l = [None]      # step whose -L/scale rows are in slot 1 of the extra k-step's tile
+    aug_d = [None]      # step whose -D rows are in slot 2
     in_flight = []      # ("Q", stage, s) or ("dO", 0, s)
     pipe = []
 
@@ -98,9 +106,11 @@ def _run(n_steps, rng, dq_free_wait=True, dk_before_dp=True, do_empty_after_dv=T
                 kind, s = op[0], op[1]
                 if kind == "S":
                     expect(q_stage[s % NQ] == s, f"S^T({s}) read Q of {q_stage[s % NQ]}")
+                    expect(aug_l[0] == s, f"S^T({s}) read -L/scale of {aug_l[0]}")
                     col_s[0] = ("S", s)
                 elif kind == "dP":
                     expect(do_stage[0] == s, f"dP^T({s}) read dO of {do_stage[0]}")
+                    expect(aug_d[0] == s, f"dP^T({s}) read -D of {aug_d[0]}")
                     col_dp[0] = ("dP", s)
                 elif kind == "dV":
                     expect(col_s[0] == ("P", s), f"dV({s}) read {col_s[0]}")
@@ -130,6 +140,7 @@ def _run(n_steps, rng, dq_free_wait=True, dk_before_dp=True, do_empty_after_dv=T
 
         if n_steps == 0:
             return
+        yield "AUG0", 0
         yield from issue_s(0)
         yield from issue_dp(0)
         for s in range(n_steps):
@@ -161,14 +172,23 @@ def _run(n_steps, rng, dq_free_wait=True, dk_before_dp=True, do_empty_after_dv=T
                     pipe.append(("commit", "FINAL"))
 
     def key_rows():
+        if n_steps:
+            aug_l[0] = aug_d[0] = 0
+            bar("AUG0").arrive()
         for s in range(n_steps):
+            if aug_early and s + 1 < n_steps:
+                aug_l[0] = s + 1  # mutation: before S^T(s) has read the slot
             yield "S", s & 1
             expect(col_s[0] == ("S", s), f"key rows read {col_s[0]} as S^T({s})")
             col_s[0] = ("P", s)
+            if s + 1 < n_steps:
+                aug_l[0] = s + 1  # the next step's -L/scale, before P(s) is handed back
             bar("P").arrive()
             yield "DP", s & 1
             expect(col_dp[0] == ("dP", s), f"key rows read {col_dp[0]} as dP^T({s})")
             ds_smem[0] = s
+            if s + 1 < n_steps:
+                aug_d[0] = s + 1  # the next step's -D, before dS^T(s) is handed back
             bar("DS").arrive()
         if n_steps:
             yield "FINAL", 0
@@ -233,4 +253,12 @@ def test_dk_after_the_next_dp_fails_in_the_model():
 
 def test_do_released_before_dv_fails_in_the_model():
     seen = _outcomes(6, do_empty_after_dv=False)
+    assert any(k != "ok" for k in seen), seen
+
+
+def test_next_steps_l_rows_written_before_s_was_read_fails_in_the_model():
+    """The key rows write the next step's -L/scale rows only after the S^T
+    they wait for has completed; written at the top of the step instead,
+    S^T can read them."""
+    seen = _outcomes(7, aug_early=True)
     assert any(k != "ok" for k in seen), seen
