@@ -454,11 +454,11 @@ __global__ void __launch_bounds__(384, 1)
     const bool key_live = key < p.N;
     const float c = p.scale_log2;
     bool ok = true;
-    // L and D of query row t of step s, loaded one step ahead from an index
-    // that is always valid (row 0 for rows past N), and left as loaded until
-    // the next step stores -L log2e and -D (negated, so that the loop below
-    // adds them; dead rows: -L = -inf so P = 0).  Nothing then waits for the
-    // loads within the step that issues them.
+    // L and D of query row t of step s, loaded during the step before from
+    // an index that is always valid (row 0 for rows past N), and left as
+    // loaded until this thread writes them as row t of the extra k-step's
+    // B operands (-L/scale and -D; dead rows -inf, so P = 0, and 0).
+    // Nothing then waits for the loads within the step that issues them.
     auto load_ld = [&](int s, float& lv, float& dv, bool& live) {
       const int g = s / per_head;
       const int qrow = (i0 + (s - g * per_head)) * C::BQ + t;
