@@ -420,7 +420,9 @@ def graph_steps(fa, torch, step, sets, flops, n=100, replays=5):
 
 def run_backward_only(args):
     """fa_backward (or the deterministic one) alone on one backward workload,
-    after one forward for O and L (used for kernel profiles)."""
+    after one forward for O and L (used for kernel profiles).  Its time (one
+    input set, calls back to back, part of it left in L2) is for orientation
+    only; the benchmark line's `bwd_workloads` are the measured figures."""
     import torch
     import exact_attention_27_gb300 as fa
     from exact_attention_27_gb300 import _build
